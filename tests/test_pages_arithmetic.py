@@ -1,0 +1,59 @@
+"""The pages' own arithmetic, reproduced from this library's row sizes.
+
+Sources: "Prime Inference: serving GLM-5.3 to agents is a KV-cache problem",
+sections "Four bits per latent value: where 352 comes from" (1.64x per row,
+(576 + x) / (352 + x) = 1.495 gives x ~ 100, 1.09M -> 1.63M tokens, 6.6 / 4.0
+GB sessions), "A kernel that reads four bits directly" (figure: staged path
+touches 352 + 576 + 576 = 1,504 B per selected row, 4.3x) and "Moving the
+cache" (5.5 GB for a 200K-token request); "GLM-5.3 PCP/DCP long-context on
+H200", section 1 footnote (26 vs 191 FLOP/B, ridge ~206) and section 3
+(54,728 B per token, 53.4 GiB at 1M tokens, 6.7 GiB with DCP8).
+"""
+import pytest
+
+import oracle as O
+
+RB4 = O.row_bytes(O.FMT_NVFP4)
+RB8 = O.row_bytes(O.FMT_FP8)
+
+
+def test_row_ratio_and_capacity_gap():
+    assert RB8 / RB4 == pytest.approx(1.64, abs=0.005)
+    # (576 + x) / (352 + x) = 1.495  =>  x = (576 - 1.495 * 352) / 0.495
+    x = (RB8 - 1.495 * RB4) / 0.495
+    assert x == pytest.approx(100, abs=1)
+    assert 1.63 / 1.09 == pytest.approx(1.495, abs=0.001)
+
+
+def test_session_sizes():
+    assert 146_000 * 78 * RB8 / 1e9 == pytest.approx(6.6, abs=0.05)
+    assert 146_000 * 78 * RB4 / 1e9 == pytest.approx(4.0, abs=0.05)
+    assert 200_000 * 78 * RB4 / 1e9 == pytest.approx(5.5, abs=0.05)
+
+
+def test_staged_path_bytes_per_row():
+    staged = RB4 + RB8 + RB8
+    assert staged == 1504
+    assert staged / RB4 == pytest.approx(4.3, abs=0.05)
+
+
+def test_indexer_key_bytes_and_per_token_budget():
+    idx_key = 128 + 4  # 128 e4m3 values plus a float32 scale
+    assert idx_key == 132
+    per_token = 78 * 656 + 21 * idx_key + 788
+    assert per_token == 54_728
+    assert per_token * 2 ** 20 / 2 ** 30 == pytest.approx(53.4, abs=0.05)
+    assert per_token * 262_144 / 2 ** 30 == pytest.approx(13.4, abs=0.05)
+    assert per_token * 2 ** 20 / 8 / 2 ** 30 == pytest.approx(6.7, abs=0.05)
+
+
+def test_flop_per_byte_accounting():
+    """2 * (576 + 512) FLOP per head per selected row (QK over 576, PV over 512)."""
+    flop_per_head_row = 2 * (576 + 512)
+    assert flop_per_head_row == 2176
+    assert 8 * flop_per_head_row / 660 == pytest.approx(26, abs=0.5)
+    assert 989 / 4.8 == pytest.approx(206, abs=0.5)
+    # The page's 191 FLOP/B for 64 heads does not follow from the same
+    # accounting (64 * 2176 / 660 = 211); this library uses its own count.
+    assert 64 * flop_per_head_row / 660 == pytest.approx(211, abs=0.5)
+    assert abs(64 * flop_per_head_row / 660 - 191) > 15
