@@ -1,0 +1,461 @@
+"""Benchmark: sparse-MLA decode rows/s per layer, HBM GB/s and % of roofline (NVFP4 vs FP8).
+
+Workload (one GPU): a TP4 decode rank -- 32 requests x 16 heads, each with a
+140,000-token paged cache (block 64, blocks scattered over one pool), top-2048
+per request (70% uniform over the prefix + 30% from the last 6,000 tokens),
+seeded synthetic data shaped like the pages' agent traffic ("Prime
+Inference: serving GLM-5.3 to agents is a KV-cache problem", sections "The
+workload" and "Decode: TP4").
+
+A step is one decode token through L layers: for each of L distinct layer
+caches (own pool, own top-k lists, own queries) one NVFP4 sparse decode.  The
+L layers are captured in one CUDA graph; their caches together are far larger
+than L2, so every layer reads its rows from HBM.  The FP8 (576-byte row)
+decode of the same rows is timed the same way and reported beside it; the
+quantize-on-write (64 sessions x 6,000 rows) and indexer + top-k (64 x 140,000
+tokens) steps of the path are timed on their own workloads in the same run.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs its own replica of the workload (requests are
+independent: weak scaling, no data-path collective); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sparse-MLA decode rows/s per layer, HBM GB/s and % of roofline (NVFP4 vs FP8)"
+UNIT = "rows/s"
+ROW_NVFP4, ROW_FP8 = 352, 576
+FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--layers", type=int, default=0, help="distinct layer caches (0: enough to defeat L2)")
+    p.add_argument("--no-extras", action="store_true", help="skip the append / indexer sub-measurements")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), \
+            "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def decode_bytes(batch, heads, topk, row_bytes):
+    """Algorithmic bytes of one decode layer: every selected row plus its int32
+    index, and per (request, head) the bf16 query (576 values), bf16 output
+    (512 values) and float lse."""
+    return batch * topk * (row_bytes + 4) + batch * heads * (576 * 2 + 512 * 2 + 4)
+
+
+def decode_flops(batch, heads, topk):
+    """2 * (576 + 512) FLOP per head per selected row (QK over 576, PV over 512)."""
+    return batch * heads * topk * 2 * (576 + 512)
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except FileNotFoundError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ reference arm (the oracle)
+def run_reference(args, rank, world):
+    import numpy as np
+    import oracle as O
+    if rank != 0:
+        return
+    batch, heads, topk, ctx = 32, 16, 2048, 140_000
+    rng = np.random.default_rng(0)
+    threads = O.host_threads()
+    # Bounded sample per step: 8 requests' decodes of one layer (float64), rows
+    # drawn and quantized by the oracle itself.
+    n_req = 8
+    qn = (rng.standard_normal((n_req, heads, 512)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    qr = (rng.standard_normal((n_req, heads, 64)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    lat = (rng.standard_normal((n_req * topk, 512)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    rope = (rng.standard_normal((n_req * topk, 64)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    nblk = n_req * topk // 64
+    pool = np.zeros(nblk * 64 * ROW_NVFP4, np.uint8)
+    O.kv_quantize_append(lat, rope, np.arange(n_req * topk, dtype=np.int64), pool, nblk, 64, 64 * ROW_NVFP4, 0)
+    bt = np.arange(nblk, dtype=np.int32).reshape(n_req, topk // 64)
+    bt_full = np.full((n_req, (ctx + 63) // 64), 0, np.int32)
+    bt_full[:, :topk // 64] = bt
+    idx = np.tile(np.arange(topk, dtype=np.int32), (n_req, 1))
+    cl = np.full(n_req, ctx, np.int32)
+
+    def step():
+        O.sparse_decode(qn, qr, pool, 64 * ROW_NVFP4, bt_full, cl, idx, 64, 1 / math.sqrt(192), 0, threads=threads)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = n_req * topk / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "TP4 rank decode, 16 heads, top-2048 rows of 352 B (float64 CPU oracle)",
+                       "sample": f"{n_req} requests x {topk} rows per step"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": f"{n_req} of 32 requests of one layer per step, {threads} host threads"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import numpy as np
+    import torch
+
+    import sparse_mla_decode_kv_gb300 as m
+    import workloads as W
+    from sparse_mla_decode_kv_gb300 import build as libbuild
+
+    libbuild.build()
+    m.load()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    hbm, tf_burst, tf_sust, peak_kind = peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    B, H, K = 32, 16, 2048
+    layer_bytes4 = decode_bytes(B, H, K, ROW_NVFP4)
+    layer_bytes8 = decode_bytes(B, H, K, ROW_FP8)
+    L = args.layers or max(8, math.ceil(4 * l2 / layer_bytes4))
+
+    def qa(lat, rope, slots, pool, nb, stride, fmt):
+        m.mla_kv_quantize_append(lat, rope, slots, pool, nb, 64, stride, fmt)
+
+    layers = []
+    for li in range(L):
+        wl = W.tp4_rank_decode(dev, seed=1000 * rank + li)
+        W.fill_pool(wl, 0, qa)
+        W.fill_pool(wl, 1, qa)
+        wl.out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=dev)
+        wl.lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+        layers.append(wl)
+    ws_bytes = m.mla_sparse_decode_workspace_size(B, H, K)
+    workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.Stream(device=dev)
+
+    def decode_all(fmt):
+        fn = m.mla_sparse_decode if fmt == 0 else m.mla_sparse_decode_fp8
+        for wl in layers:
+            fn(wl.q_nope, wl.q_rope, wl.pools[fmt], wl.strides[fmt], wl.num_blocks, wl.block_table,
+               wl.context_lens, wl.topk_idx, wl.softmax_scale, out=wl.out, lse=wl.lse, workspace=workspace,
+               stream=stream)
+
+    def capture(fmt):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            decode_all(fmt)  # warm the launch path outside capture
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                decode_all(fmt)
+        return g
+
+    graphs = {0: capture(0), 1: capture(1)}
+    torch.cuda.synchronize()
+
+    def timed(g, steps, warmup):
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                g.replay()
+        stream.synchronize()
+        if pg:
+            pg.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps):
+                g.replay()
+            e1.record(stream)
+        e1.synchronize()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        if pg:
+            t = torch.tensor([ms], device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            ms = float(t)
+        return ms
+
+    with ClockSampler(local) as clocks:
+        ms4 = timed(graphs[0], args.steps, args.warmup)
+        ms8 = timed(graphs[1], args.steps, args.warmup)
+    clk = clocks.summary()
+    splits = m.mla_sparse_decode_workspace_size(B, H, K) > 0
+    launches_per_step = L * (2 if splits else 1)
+
+    per_layer4 = ms4 / L * 1e-3
+    per_layer8 = ms8 / L * 1e-3
+    rows = B * K
+    value = rows * world / per_layer4
+    ach4 = layer_bytes4 / per_layer4 / 1e9
+    ach8 = layer_bytes8 / per_layer8 / 1e9
+    fl = decode_flops(B, H, K)
+    roof_t4 = max(layer_bytes4 / (hbm * 1e9), fl / (tf_burst * 1e12))
+    roof_t8 = max(layer_bytes8 / (hbm * 1e9), fl / (tf_burst * 1e12))
+
+    # ---- end to end through the C ABI with host buffers (pinned), per layer:
+    # H2D q_nope, q_rope, top-k list, context lengths; decode; D2H out + lse.
+    host = []
+    for wl in layers:
+        host.append({k: getattr(wl, k).cpu().pin_memory() for k in ("q_nope", "q_rope", "topk_idx", "context_lens")})
+    h_out = torch.empty((B, H, 512), dtype=torch.bfloat16).pin_memory()
+    h_lse = torch.empty((B, H), dtype=torch.float32).pin_memory()
+    d_in = {k: torch.empty_like(v, device=dev) for k, v in host[0].items()}
+    h2d = sum(v.numel() * v.element_size() for v in host[0].values()) * L
+    d2h = (h_out.numel() * 2 + h_lse.numel() * 4) * L
+
+    def e2e_step():
+        for li, wl in enumerate(layers):
+            for k, v in host[li].items():
+                d_in[k].copy_(v, non_blocking=True)
+            m.mla_sparse_decode(d_in["q_nope"], d_in["q_rope"], wl.pools[0], wl.strides[0], wl.num_blocks,
+                                wl.block_table, d_in["context_lens"], d_in["topk_idx"], wl.softmax_scale,
+                                out=wl.out, lse=wl.lse, workspace=workspace, stream=stream)
+            h_out.copy_(wl.out, non_blocking=True)
+            h_lse.copy_(wl.lse, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            e2e_step()
+        stream.synchronize()
+        if pg:
+            pg.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+    e1.synchronize()
+    ms_e2e = e0.elapsed_time(e1) / args.steps
+    if pg:
+        t = torch.tensor([ms_e2e], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms_e2e = float(t)
+    e2e_value = rows * L * world / (ms_e2e * 1e-3)
+
+    extras = {}
+    if not args.no_extras:
+        del graphs
+        extras = sub_measurements(m, W, dev, stream, args, hbm)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms4, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": "TP4 rank decode: 32 requests x 16 heads, 140,000-token contexts, top-2048 "
+                               "(70% prefix + 30% last 6,000), NVFP4 352-byte rows, block 64",
+                   "layers_per_step": L, "l2": f"inputs larger than L2: {L} distinct layer caches, "
+                                              f"{L * layer_bytes4 / 1e6:.0f} MB read per step vs "
+                                              f"{l2 / 1e6:.0f} MB L2",
+                   "global_batch": B * world, "seq_len": 140_000, "parallelism": f"replicas x{world}"},
+        "per_layer_us": per_layer4 * 1e6,
+        "hbm_gbs": ach4,
+        "roofline": {"bound": "hbm" if layer_bytes4 / hbm / 1e9 >= fl / tf_burst / 1e12 else "tensor",
+                     "achieved": ach4, "peak": hbm, "unit": "GB/s", "frac": ach4 / hbm, "traffic": None,
+                     "kernel": "sparse_decode_kernel<NVFP4> + splitk_merge_kernel (one decode layer)",
+                     "algorithmic_bytes_per_launch": layer_bytes4, "peak_source": peak_kind,
+                     "roofline_us": roof_t4 * 1e6, "frac_of_roofline_time": roof_t4 / per_layer4,
+                     "vs_nominal_8tbs": ach4 / 8000.0},
+        "fp8": {"value": rows * world / per_layer8, "unit": UNIT, "per_layer_us": per_layer8 * 1e6,
+                "hbm_gbs": ach8, "frac": ach8 / hbm, "roofline_us": roof_t8 * 1e6,
+                "bytes_per_row": ROW_FP8 + 4},
+        "nvfp4_bytes_per_row": ROW_NVFP4 + 4,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    line.update(extras)
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline(m, W, dev)
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+def sub_measurements(m, W, dev, stream, args, hbm):
+    """Quantize-on-write and indexer + top-k, each timed with CUDA events."""
+    import torch
+    out = {}
+    wl = W.append_turn(dev)
+    n = wl.slot_mapping.numel()
+    res = {}
+    for fmt, rb in ((0, ROW_NVFP4), (1, ROW_FP8)):
+        stride = 64 * rb
+        pool = torch.zeros(wl.num_blocks * stride, dtype=torch.uint8, device=dev)
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                m.mla_kv_quantize_append(wl.latent, wl.rope, wl.slot_mapping, pool, wl.num_blocks, 64, stride, fmt,
+                                         stream=stream)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.steps):
+                m.mla_kv_quantize_append(wl.latent, wl.rope, wl.slot_mapping, pool, wl.num_blocks, 64, stride, fmt,
+                                         stream=stream)
+            e1.record(stream)
+        e1.synchronize()
+        t = e0.elapsed_time(e1) / args.steps * 1e-3
+        bytes_ = n * (512 * 2 + 64 * 2 + 8 + rb)
+        res["nvfp4" if fmt == 0 else "fp8"] = {"rows_per_s": n / t, "us": t * 1e6, "hbm_gbs": bytes_ / t / 1e9,
+                                               "frac": bytes_ / t / 1e9 / hbm}
+        del pool
+    out["append"] = {"workload": wl.name, **res}
+    del wl
+    torch.cuda.empty_cache()
+
+    iw = W.indexer_keys(dev, seed=0, batch=64, ctx=140_000, n_heads=32, topk=2048)
+    max_ctx = 140_000
+    ws = torch.empty(m.mla_indexer_topk_workspace_size(64, max_ctx, 2048), dtype=torch.uint8, device=dev)
+    tk = torch.empty((64, 2048), dtype=torch.int32, device=dev)
+
+    def run():
+        m.mla_indexer_topk(iw.q_idx, iw.head_w, iw.key_pool, iw.key_stride, iw.num_blocks, iw.block_table,
+                           iw.context_lens, 2048, max_ctx, topk_out=tk, workspace=ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            run()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            run()
+        e1.record(stream)
+    e1.synchronize()
+    t = e0.elapsed_time(e1) / args.steps * 1e-3
+    tokens = 64 * 140_000
+    key_bytes = tokens * 132
+    out["indexer_topk"] = {"workload": iw.name, "us": t * 1e6, "tokens_per_s": tokens / t,
+                           "key_hbm_gbs": key_bytes / t / 1e9, "frac": key_bytes / t / 1e9 / hbm}
+    return out
+
+
+def cpu_baseline(m, W, dev):
+    """The float64 oracle on a bounded sample of the same workload (4 requests
+    of one layer), on all host cores."""
+    import numpy as np
+    import torch
+    import oracle as O
+
+    def u16(t):
+        return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+    wl = W.tp4_rank_decode(dev, seed=0)
+    reqs = list(range(wl.batch))
+    threads = O.host_threads()
+    pools, qn, qr = [], u16(wl.q_nope[reqs]), u16(wl.q_rope[reqs])
+    K = wl.topk
+    nblk = K // 64
+    pool = np.zeros(len(reqs) * nblk * 64 * ROW_NVFP4, np.uint8)
+    for i, b in enumerate(reqs):
+        lat, rope = wl.request_rows(b, wl.topk_idx[b])
+        O.kv_quantize_append(u16(lat), u16(rope), np.arange(i * K, (i + 1) * K, dtype=np.int64), pool,
+                             len(reqs) * nblk, 64, 64 * ROW_NVFP4, 0)
+    bt = np.arange(len(reqs) * nblk, dtype=np.int32).reshape(len(reqs), nblk)
+    idx = np.tile(np.arange(K, dtype=np.int32), (len(reqs), 1))
+    cl = np.full(len(reqs), K, np.int32)
+    # Repeat whole-layer decodes until about 10 s of CPU time (threads x wall) is spent.
+    reps, t_total = 0, 0.0
+    while reps < 20 and t_total * threads < 10.0:
+        t0 = time.perf_counter()
+        O.sparse_decode(qn, qr, pool, 64 * ROW_NVFP4, bt, cl, idx, 64, wl.softmax_scale, 0, threads=threads)
+        t_total += time.perf_counter() - t0
+        reps += 1
+    return {"value": reps * len(reqs) * K / t_total, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{reps} x one layer ({len(reqs)} requests x {K} rows of 352 B), float64, "
+                      f"{t_total:.2f} s wall on {threads} threads"}
+
+
+if __name__ == "__main__":
+    main()

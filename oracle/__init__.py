@@ -70,7 +70,7 @@ def lib():
         L.oracle_quantize_row_fp8.argtypes = [P, P, P]
         L.oracle_dequant_row.restype = None
         L.oracle_dequant_row.argtypes = [P, i32, P, P]
-        L.oracle_kv_quantize_append.restype = i32
+        L.oracle_kv_quantize_append.restype = i64
         L.oracle_kv_quantize_append.argtypes = [P, P, P, i64, P, i64, i32, i64, i32]
         L.oracle_sparse_decode_request.restype = None
         L.oracle_sparse_decode_request.argtypes = [P, P, P, i64, P, i32, P, i32, i32, i32, f64, i32, P, P]
@@ -150,8 +150,11 @@ def dequant_row(row: np.ndarray, fmt: int):
 
 
 def kv_quantize_append(latent, rope, slot_mapping, kv_pool: np.ndarray, num_blocks: int,
-                       block_size: int, kv_block_stride: int, fmt: int) -> None:
-    """Quantize-on-write into ``kv_pool`` (uint8, flat or shaped), in place."""
+                       block_size: int, kv_block_stride: int, fmt: int) -> int:
+    """Quantize-on-write into ``kv_pool`` (uint8, flat or shaped), in place.
+
+    Tokens whose slot is negative or past the pool are skipped; returns how
+    many were skipped."""
     lat = np.ascontiguousarray(latent, dtype=np.uint16)
     rp = np.ascontiguousarray(rope, dtype=np.uint16)
     sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
@@ -159,10 +162,8 @@ def kv_quantize_append(latent, rope, slot_mapping, kv_pool: np.ndarray, num_bloc
     assert lat.size == n * LATENT and rp.size == n * ROPE
     assert kv_pool.dtype == np.uint8 and kv_pool.flags["C_CONTIGUOUS"]
     assert kv_pool.size >= num_blocks * kv_block_stride
-    rc = lib().oracle_kv_quantize_append(_ptr(lat), _ptr(rp), _ptr(sm), n, _ptr(kv_pool), num_blocks,
-                                         block_size, kv_block_stride, fmt)
-    if rc != 0:
-        raise ValueError("slot outside the pool")
+    return int(lib().oracle_kv_quantize_append(_ptr(lat), _ptr(rp), _ptr(sm), n, _ptr(kv_pool), num_blocks,
+                                               block_size, kv_block_stride, fmt))
 
 
 # ---------------------------------------------------------------- decode

@@ -217,27 +217,26 @@ void oracle_dequant_row(const uint8_t* row, int fmt, double* c, double* r) {
 
 /* Quantize-on-write of n_tokens rows into a paged pool: token n goes to
  * slot = slot_mapping[n] (block = slot / block_size, offset = slot %
- * block_size); a negative slot is skipped.  Returns -1 if a slot names a
- * block outside [0, num_blocks), else 0 (nothing is written in that case). */
-int oracle_kv_quantize_append(const uint16_t* latent, const uint16_t* rope, const int64_t* slot_mapping,
-                              int64_t n_tokens, uint8_t* kv_pool, int64_t num_blocks, int block_size,
-                              int64_t kv_block_stride, int fmt) {
+ * block_size).  A negative slot, or one whose block is outside
+ * [0, num_blocks), is skipped.  Returns the number of skipped tokens. */
+int64_t oracle_kv_quantize_append(const uint16_t* latent, const uint16_t* rope, const int64_t* slot_mapping,
+                                  int64_t n_tokens, uint8_t* kv_pool, int64_t num_blocks, int block_size,
+                                  int64_t kv_block_stride, int fmt) {
   size_t rb = oracle_row_bytes(fmt);
+  int64_t skipped = 0;
   for (int64_t n = 0; n < n_tokens; n++) {
     int64_t slot = slot_mapping[n];
-    if (slot < 0) continue;
-    if (slot / block_size >= num_blocks) return -1;
-  }
-  for (int64_t n = 0; n < n_tokens; n++) {
-    int64_t slot = slot_mapping[n];
-    if (slot < 0) continue;
+    if (slot < 0 || slot / block_size >= num_blocks) {
+      skipped++;
+      continue;
+    }
     uint8_t* row = kv_pool + (slot / block_size) * kv_block_stride + (slot % block_size) * (int64_t)rb;
     if (fmt == 0)
       oracle_quantize_row_nvfp4(latent + n * ORACLE_LATENT, rope + n * ORACLE_ROPE, row);
     else
       oracle_quantize_row_fp8(latent + n * ORACLE_LATENT, rope + n * ORACLE_ROPE, row);
   }
-  return 0;
+  return skipped;
 }
 
 /* ------------------------------------------------------------------------ */

@@ -1,0 +1,179 @@
+// Device-side helpers shared by the library's kernels: row layout constants,
+// inline-PTX conversions, warp-level tensor-core MMA, bulk async copies and
+// bounded mbarrier waits.  sm_103a only.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+namespace mla {
+
+// ---- row layout ("Prime Inference", section "Four bits per latent value":
+// 512 x 4 bit codes + 32 one-byte scales + 64 one-byte rope = 352 bytes; the
+// FP8 row is 512 + 64 bytes).  Offsets inside the row are this library's.
+constexpr int kLatent = 512;
+constexpr int kRope = 64;
+constexpr int kGroup = 16;                 // latent values per e4m3 scale
+constexpr int kRowNvfp4 = 352;
+constexpr int kRowFp8 = 576;
+constexpr int kScaleOff = 256;             // NVFP4: scales after the codes
+constexpr int kRopeOffNvfp4 = 288;
+constexpr int kRopeOffFp8 = 512;
+constexpr int kBlock = 64;                 // tokens per paged block
+constexpr int kIdxDim = 128;               // indexer key width (e4m3)
+
+// Bits of the library-wide device fault word (a __device__ variable in
+// mla_api.cu whose address kernels receive as an argument).
+constexpr unsigned int kFaultDecodeWait = 1u;
+constexpr unsigned int kFaultIndexerWait = 2u;
+// Poll budget of a bounded wait (each poll backs off ~32-256 ns): on the
+// order of a second, far beyond any legitimate wait in these kernels.
+constexpr uint32_t kWaitPolls = 1u << 23;
+
+// ---- conversions -----------------------------------------------------------
+// Two e2m1 codes (low nibble -> low half) to two exact f16 values.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t d;
+  asm("{ .reg .b8 b; cvt.u8.u32 b, %1; cvt.rn.f16x2.e2m1x2 %0, b; }" : "=r"(d) : "r"(byte));
+  return d;
+}
+// Two e4m3 bytes (low byte -> low half) to two exact f16 values.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
+  uint32_t d;
+  uint16_t h = static_cast<uint16_t>(two_bytes);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(h));
+  return d;
+}
+// Two floats to e4m3, round-to-nearest-even, satfinite.  `hi` lands in the
+// high byte, `lo` in the low byte.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float hi, float lo) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Two floats to e2m1, round-to-nearest-even, satfinite.  `hi` lands in the
+// high nibble, `lo` in the low nibble; the sign of a value that rounds to
+// zero is kept (code 0x8).
+__device__ __forceinline__ uint32_t f32x2_to_e2m1x2(float hi, float lo) {
+  uint32_t r;
+  asm("{ .reg .b8 b; cvt.rn.satfinite.e2m1x2.f32 b, %1, %2; cvt.u32.u8 %0, b; }" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Two floats to f16x2 (lo -> low half), round-to-nearest-even, saturating at
+// +-65504.
+__device__ __forceinline__ uint32_t f32x2_to_f16x2_sat(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ---- warp-level tensor core (m16n8k16, f16 x f16 -> f32) -------------------
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Transpose of an 8x8 16-bit tile held in the standard fragment layout
+// (lane l holds row l/4, columns 2(l%4) and 2(l%4)+1).
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t smem_addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_addr));
+}
+
+// ---- shared memory, mbarriers and bulk copies -----------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{ .reg .b64 st; mbarrier.arrive.release.cta.shared::cta.b64 st, [%0]; }" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("{ .reg .b64 st; mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 st, [%0], %1; }" ::"r"(
+                   smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase with the given parity.  Returns false (after
+// setting `fault` in *fault_word) if it never completed.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned int* fault_word,
+                                                  unsigned int fault) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint32_t ns = 32;
+  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+    __nanosleep(ns);
+    if (ns < 256) ns <<= 1;
+    if (mbar_try_wait(bar, parity)) return true;
+  }
+  atomicOr(fault_word, fault);
+  return false;
+}
+// One contiguous global -> shared copy, completing bytes on `bar`.  Both
+// addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint2 lds_u64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+}  // namespace mla

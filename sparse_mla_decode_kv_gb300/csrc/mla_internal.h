@@ -1,0 +1,42 @@
+// Host-side declarations shared between the C-ABI layer (mla_api.cu) and the
+// kernel translation units.  Not part of the public interface.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mla {
+
+// Multiprocessor count of the current device (cached per device).
+int device_sm_count();
+// Device address of the library's fault word on the current device.
+unsigned int* fault_word_ptr();
+
+cudaError_t launch_quantize_append(const uint16_t* latent, const uint16_t* rope, const int64_t* slot_mapping,
+                                   int64_t n_tokens, void* pool, int64_t num_blocks, int64_t block_stride, int fmt,
+                                   cudaStream_t stream);
+
+// Sparse decode: split plan and launch.
+struct DecodePlan {
+  int splits;          // CTAs per (request, 16-head group) along the top-k list
+  int rows_per_split;  // multiple of 16
+  size_t workspace;    // bytes of split partials (0 when splits == 1)
+};
+DecodePlan plan_sparse_decode(int batch, int num_heads, int topk);
+cudaError_t launch_sparse_decode(int fmt, const uint16_t* q_nope, const uint16_t* q_rope, const void* pool,
+                                 int64_t block_stride, int64_t num_blocks, const int32_t* block_table,
+                                 int max_blocks_per_req, const int32_t* context_lens, const int32_t* topk_idx,
+                                 int batch, int num_heads, int topk, float softmax_scale, uint16_t* out, float* lse,
+                                 void* workspace, const DecodePlan& plan, cudaStream_t stream);
+
+// Indexer and top-k.
+size_t topk_workspace_bytes(int batch, int max_context_len, int topk);
+cudaError_t launch_topk(const float* scores, int64_t row_stride, const int32_t* context_lens, int batch, int topk,
+                        int max_context_len, int32_t* out, void* workspace, cudaStream_t stream);
+cudaError_t launch_indexer_scores(const uint16_t* q_idx, const float* head_w, const void* key_pool,
+                                  int64_t block_stride, int64_t num_blocks, const int32_t* block_table,
+                                  int max_blocks_per_req, const int32_t* context_lens, int batch, int n_heads,
+                                  int max_context_len, float* scores, int64_t scores_stride, cudaStream_t stream);
+
+}  // namespace mla

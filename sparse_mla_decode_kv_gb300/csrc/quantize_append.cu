@@ -1,0 +1,98 @@
+// Quantize-on-write of MLA latent rows into the paged cache.
+//
+// "Prime Inference: serving GLM-5.3 to agents is a KV-cache problem",
+// section "Four bits per latent value": the 512-value latent is stored as
+// four-bit values with one FP8 scale per 16 values, the 64 rope values stay
+// FP8, 576 -> 352 bytes per row.  The FP8 comparison row keeps all 576 values
+// as e4m3 with no scale.
+//
+// One warp per token.  Lane g owns latent group g (16 values, 32 bytes of
+// bf16) and rope values 2g, 2g+1, so the warp reads its 1,152 input bytes
+// with fully used 16-byte loads and writes the 352 (or 576) output bytes as
+// contiguous 8-, 1- and 2-byte lanes.  The kernel is HBM-bound: 1,160 bytes
+// in (latent + rope + slot) and 352 out per token.
+#include "mla_device.cuh"
+#include "mla_internal.h"
+
+namespace mla {
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+
+template <int FMT>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+    quantize_append_kernel(const uint16_t* __restrict__ latent, const uint16_t* __restrict__ rope,
+                           const int64_t* __restrict__ slot_mapping, int64_t n_tokens, uint8_t* __restrict__ pool,
+                           int64_t num_blocks, int64_t block_stride) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp_global = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int64_t warp_stride = static_cast<int64_t>(gridDim.x) * kWarpsPerBlock;
+  for (int64_t n = warp_global; n < n_tokens; n += warp_stride) {
+    const int64_t slot = __ldg(slot_mapping + n);
+    if (slot < 0 || slot / kBlock >= num_blocks) continue;  // skipped (warp-uniform)
+    uint8_t* row = pool + (slot / kBlock) * block_stride + (slot % kBlock) * (FMT == 0 ? kRowNvfp4 : kRowFp8);
+
+    // 16 latent values of group `lane`, as two 16-byte loads.
+    const uint4* src = reinterpret_cast<const uint4*>(latent + n * kLatent + lane * kGroup);
+    const uint4 v0 = __ldg(src);
+    const uint4 v1 = __ldg(src + 1);
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      x[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
+      x[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+    }
+    const uint32_t rope2 = __ldg(reinterpret_cast<const uint32_t*>(rope + n * kRope) + lane);
+    const uint32_t rope_e4m3x2 = f32x2_to_e4m3x2(bf16_bits_to_f32(rope2 >> 16), bf16_bits_to_f32(rope2 & 0xFFFFu));
+
+    if constexpr (FMT == 0) {
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+      // S = e4m3(amax / 6): IEEE division, then round-to-nearest-even.
+      const uint32_t s_code = f32x2_to_e4m3x2(0.f, __fdiv_rn(amax, 6.0f)) & 0xFFu;
+      const uint32_t s_f16 = e4m3x2_to_f16x2(s_code) & 0xFFFFu;
+      const float s = __half2float(__ushort_as_half(static_cast<unsigned short>(s_f16)));
+      uint32_t lo = 0, hi = 0;  // 16 codes: element 2i in the low nibble of byte i
+      if (s_code != 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          lo |= f32x2_to_e2m1x2(__fdiv_rn(x[2 * i + 1], s), __fdiv_rn(x[2 * i], s)) << (8 * i);
+          hi |= f32x2_to_e2m1x2(__fdiv_rn(x[8 + 2 * i + 1], s), __fdiv_rn(x[8 + 2 * i], s)) << (8 * i);
+        }
+      }
+      *reinterpret_cast<uint2*>(row + lane * 8) = make_uint2(lo, hi);
+      row[kScaleOff + lane] = static_cast<uint8_t>(s_code);
+      *reinterpret_cast<uint16_t*>(row + kRopeOffNvfp4 + 2 * lane) = static_cast<uint16_t>(rope_e4m3x2);
+    } else {
+      uint32_t b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        b[i] = f32x2_to_e4m3x2(x[4 * i + 1], x[4 * i]) | (f32x2_to_e4m3x2(x[4 * i + 3], x[4 * i + 2]) << 16);
+      *reinterpret_cast<uint4*>(row + lane * 16) = make_uint4(b[0], b[1], b[2], b[3]);
+      *reinterpret_cast<uint16_t*>(row + kRopeOffFp8 + 2 * lane) = static_cast<uint16_t>(rope_e4m3x2);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_append(const uint16_t* latent, const uint16_t* rope, const int64_t* slot_mapping,
+                                   int64_t n_tokens, void* pool, int64_t num_blocks, int64_t block_stride, int fmt,
+                                   cudaStream_t stream) {
+  if (n_tokens <= 0) return cudaSuccess;
+  int sms = device_sm_count();
+  int64_t want = (n_tokens + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  int64_t cap = static_cast<int64_t>(sms) * 16;  // grid-stride beyond 16 blocks per SM
+  int grid = static_cast<int>(want < cap ? want : cap);
+  if (fmt == 0)
+    quantize_append_kernel<0><<<grid, kWarpsPerBlock * 32, 0, stream>>>(
+        latent, rope, slot_mapping, n_tokens, static_cast<uint8_t*>(pool), num_blocks, block_stride);
+  else
+    quantize_append_kernel<1><<<grid, kWarpsPerBlock * 32, 0, stream>>>(
+        latent, rope, slot_mapping, n_tokens, static_cast<uint8_t*>(pool), num_blocks, block_stride);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -1,0 +1,119 @@
+"""The C-ABI library builds, loads and exports every symbol include/mla_nvfp4.h
+declares; host-side validation rejects bad arguments before any launch.
+
+CPU only: no call here reaches a CUDA launch (every call below fails
+validation, or is a pure host query)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mla_nvfp4.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_mla_decode_kv_gb300 import build
+    build.build()
+    import sparse_mla_decode_kv_gb300 as m
+    return m.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported_and_bound(lib):
+    import sparse_mla_decode_kv_gb300 as m
+    names = declared_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared but not exported"
+        assert n in m.SIGNATURES, f"{n} has no Python binding"
+    assert set(m.SIGNATURES) == set(names)
+
+
+def test_row_bytes_and_status_strings(lib):
+    assert lib.mla_kv_row_bytes(0) == 352
+    assert lib.mla_kv_row_bytes(1) == 576
+    assert lib.mla_kv_row_bytes(7) == 0
+    assert lib.mla_status_string(0) == b"MLA_OK"
+    assert lib.mla_status_string(3) == b"MLA_ERR_WORKSPACE_TOO_SMALL"
+    err = C.c_int(-1)
+    assert lib.mla_last_cuda_error(C.byref(err)) == 0 and err.value == 0
+    assert lib.mla_last_cuda_error(None) == 1
+
+
+FAKE = C.c_void_p(0x10000)  # never dereferenced: every call below fails validation first
+
+
+def decode_call(lib, **over):
+    a = dict(q_nope=FAKE, q_rope=FAKE, pool=FAKE, stride=64 * 352, num_blocks=10, bt=FAKE, max_blocks=4, cl=FAKE,
+             idx=FAKE, batch=2, heads=16, bs=64, topk=2048, scale=0.07, out=FAKE, lse=None, ws=None, ws_bytes=0)
+    a.update(over)
+    return lib.mla_sparse_decode(a["q_nope"], a["q_rope"], a["pool"], a["stride"], a["num_blocks"], a["bt"],
+                                 a["max_blocks"], a["cl"], a["idx"], a["batch"], a["heads"], a["bs"], a["topk"],
+                                 a["scale"], a["out"], a["lse"], a["ws"], a["ws_bytes"], None)
+
+
+def test_decode_validation(lib):
+    INVALID, UNSUPPORTED = 1, 2
+    assert decode_call(lib, q_nope=None) == INVALID
+    assert decode_call(lib, out=None) == INVALID
+    assert decode_call(lib, bs=32) == UNSUPPORTED
+    assert decode_call(lib, bs=48) == INVALID
+    assert decode_call(lib, heads=8) == INVALID
+    assert decode_call(lib, heads=24) == INVALID
+    assert decode_call(lib, heads=144) == INVALID
+    assert decode_call(lib, topk=0) == INVALID
+    assert decode_call(lib, topk=2049) == INVALID
+    assert decode_call(lib, scale=float("nan")) == INVALID
+    assert decode_call(lib, stride=64 * 352 - 16) == INVALID
+    assert decode_call(lib, stride=64 * 352 + 8) == INVALID
+    assert decode_call(lib, pool=C.c_void_p(0x10008)) == INVALID  # pool not 16-byte aligned
+    assert decode_call(lib, batch=-1) == INVALID
+    assert decode_call(lib, max_blocks=0) == INVALID
+    assert decode_call(lib, batch=0, q_nope=None) == 0  # empty batch is a no-op
+
+
+def test_quantize_append_validation(lib):
+    f = lib.mla_kv_quantize_append
+    assert f(FAKE, FAKE, FAKE, 10, FAKE, 4, 64, 64 * 352, 2, None) == 1        # bad format
+    assert f(FAKE, FAKE, FAKE, 10, FAKE, 4, 64, 64 * 352 - 16, 0, None) == 1   # stride too small
+    assert f(FAKE, FAKE, FAKE, 10, FAKE, 4, 64, 64 * 576 - 16, 1, None) == 1
+    assert f(FAKE, FAKE, FAKE, 10, FAKE, 4, 128, 128 * 352, 0, None) == 2      # block size unsupported
+    assert f(None, FAKE, FAKE, 10, FAKE, 4, 64, 64 * 352, 0, None) == 1
+    assert f(C.c_void_p(0x10004), FAKE, FAKE, 10, FAKE, 4, 64, 64 * 352, 0, None) == 1  # latent misaligned
+    assert f(None, None, None, 0, None, 4, 64, 64 * 352, 0, None) == 0         # n_tokens == 0 is a no-op
+    assert f(FAKE, FAKE, FAKE, -1, FAKE, 4, 64, 64 * 352, 0, None) == 1
+
+
+def test_topk_and_indexer_validation(lib):
+    assert lib.mla_topk(FAKE, 100, FAKE, 2, 0, 100, FAKE, None, 0, None) == 1
+    assert lib.mla_topk(FAKE, 100, FAKE, 2, 2049, 100, FAKE, None, 0, None) == 1
+    assert lib.mla_topk(FAKE, 99, FAKE, 2, 16, 100, FAKE, None, 0, None) == 1   # stride < max_context_len
+    assert lib.mla_topk(None, 100, FAKE, 2, 16, 100, FAKE, None, 0, None) == 1
+    assert lib.mla_topk(None, 100, None, 0, 16, 100, None, None, 0, None) == 0  # empty batch
+    f = lib.mla_indexer_topk
+    args = [FAKE, FAKE, FAKE, 64 * 132, 10, FAKE, 4, FAKE, 2, 32, 64, 2048, FAKE, None, 4096, None, 0, None]
+    bad_heads = list(args)
+    bad_heads[9] = 24
+    assert f(*bad_heads) == 2
+    bad_heads[9] = 7
+    assert f(*bad_heads) == 1
+    small_stride = list(args)
+    small_stride[3] = 64 * 132 - 16
+    assert f(*small_stride) == 1
+    no_ws = list(args)
+    assert f(*no_ws) == 3  # the scores need workspace
+    assert lib.mla_indexer_topk_workspace_size(2, 4096, 2048) >= 2 * 4096 * 4
+
+
+def test_workspace_sizes_are_zero_for_empty_or_invalid(lib):
+    assert lib.mla_sparse_decode_workspace_size(0, 16, 2048) == 0
+    assert lib.mla_sparse_decode_workspace_size(4, 8, 2048) == 0
+    assert lib.mla_topk_workspace_size(0, 10, 10) == 0

@@ -1,0 +1,167 @@
+"""Indexer score and exact top-k on the GPU against the oracle.
+
+Sources: "GLM-5.3 PCP/DCP long-context on H200", section 1 (an indexer
+scores every earlier token; sparse MLA attends to the top 2,048) and section
+3 (keys: 128 FP8 values plus a 4-byte scale per token); "Prime Inference:
+serving GLM-5.3 to agents is a KV-cache problem", section "Decode: TP4"
+(index_topk 2048).
+
+Contract (the score is float32 on the GPU, float64 in the oracle):
+  * top-k selection is exact: on synthetic float32 scores fed to both sides
+    (mla_topk), the index sets are identical, ties going to the lower index;
+  * scores are within 1e-5 (1 + |ref|) of the oracle;
+  * the chained top-k equals the exact top-k of the GPU's own scores (checked
+    with numpy, not the oracle), and differs from the oracle's top-k only by
+    swaps whose two float64 scores lie within that band of the k-th score."""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+from gpu_helpers import assert_decode_close, lib, oracle_rows_decode, u16
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+SCORE_TOL = 1e-5
+
+
+def gpu_topk(m, scores: np.ndarray, lens, k):
+    s = torch.from_numpy(np.ascontiguousarray(scores, dtype=np.float32)).to(DEV)
+    cl = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    out = m.mla_topk(s, cl, k)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def lexsort_topk(scores: np.ndarray, k: int) -> np.ndarray:
+    s = scores.astype(np.float64) + 0.0  # -0.0 -> +0.0
+    order = np.lexsort((np.arange(s.size), -s))
+    sel = np.sort(order[:min(k, s.size)])
+    out = np.full(k, -1, np.int32)
+    out[:sel.size] = sel
+    return out
+
+
+@pytest.mark.parametrize("case", ["normal", "ties", "all_equal", "signed_zero", "negative", "tiny_ctx",
+                                  "ctx_eq_k", "ctx_k_plus_1", "empty", "huge_range"])
+def test_topk_exact_on_synthetic_scores(case):
+    m = lib()
+    rng = np.random.default_rng(zlib.crc32(case.encode()))
+    B, L, k = 6, 20_000, 2048
+    lens = [L, L - 3, 12_345, 4096, 2049, 2048]
+    s = rng.standard_normal((B, L)).astype(np.float32) * 30 + 70
+    if case == "ties":
+        s = rng.integers(0, 40, (B, L)).astype(np.float32) * 0.25
+    elif case == "all_equal":
+        s[:] = 1.5
+    elif case == "signed_zero":
+        s = np.where(rng.random((B, L)) < 0.5, np.float32(0.0), np.float32(-0.0)).astype(np.float32)
+        s[:, ::97] = 1.0
+    elif case == "negative":
+        s = -np.abs(s)
+    elif case == "tiny_ctx":
+        lens = [1, 0, 5, 2047, 100, 3]
+    elif case == "ctx_eq_k":
+        lens = [k] * B
+    elif case == "ctx_k_plus_1":
+        lens = [k + 1] * B
+    elif case == "empty":
+        lens = [0] * B
+    elif case == "huge_range":
+        s = (rng.standard_normal((B, L)) * np.exp(rng.uniform(-80, 80, (B, L)))).astype(np.float32)
+    got = gpu_topk(m, s, lens, k)
+    for b in range(B):
+        ref = O.topk(s[b, :lens[b]], k)
+        assert np.array_equal(got[b], ref), f"request {b}"
+
+
+def oracle_scores(wl, requests, threads):
+    return O.indexer_scores(u16(wl.q_idx), wl.head_w.cpu().numpy(), wl.key_pool.cpu().numpy(), wl.key_stride,
+                            wl.block_table.cpu().numpy(), wl.context_lens.cpu().numpy(), 64, requests=requests,
+                            threads=threads)
+
+
+def run_indexer(m, wl, max_ctx):
+    scores = torch.full((wl.q_idx.shape[0], max_ctx), float("nan"), dtype=torch.float32, device=DEV)
+    topk, _ = m.mla_indexer_topk(wl.q_idx, wl.head_w, wl.key_pool, wl.key_stride, wl.num_blocks, wl.block_table,
+                                 wl.context_lens, wl.topk, max_ctx, scores_out=scores)
+    torch.cuda.synchronize()
+    return topk.cpu().numpy(), scores.cpu().numpy()
+
+
+def check_request(got_idx, got_scores, ref_scores, k):
+    n = ref_scores.size
+    gs = got_scores[:n].astype(np.float64)
+    assert np.all(np.abs(gs - ref_scores) <= SCORE_TOL * (1 + np.abs(ref_scores))), "score accuracy"
+    # selection exactness on the GPU's own scores (numpy, not the oracle)
+    assert np.array_equal(got_idx, lexsort_topk(got_scores[:n], k)), "top-k of the GPU's scores"
+    # against the float64 top-k: only near-tie swaps at the boundary are allowed
+    ref_idx = O.topk(ref_scores, k)
+    a, b = set(got_idx[got_idx >= 0].tolist()), set(ref_idx[ref_idx >= 0].tolist())
+    if a == b:
+        return 0
+    kth = np.sort(ref_scores)[::-1][min(k, n) - 1]
+    band = SCORE_TOL * (1 + abs(kth)) * 2
+    for t in a ^ b:
+        assert abs(ref_scores[t] - kth) <= band, f"swap of token {t} outside the tie band"
+    return len(a ^ b) // 2
+
+
+@pytest.mark.parametrize("nh,lens", [(32, [3000, 130, 64, 1]), (8, [5000, 4999]), (16, [2048, 2500]),
+                                     (64, [1000, 777])])
+def test_indexer_small(nh, lens):
+    m = lib()
+    wl = W.indexer_keys(DEV, seed=nh, batch=len(lens), n_heads=nh, topk=512, ctx_lens=lens)
+    max_ctx = max(lens) + 7
+    idx, sc = run_indexer(m, wl, max_ctx)
+    ref = oracle_scores(wl, None, 1)
+    for b in range(len(lens)):
+        check_request(idx[b], sc[b], ref[b], wl.topk)
+        assert np.all(np.isnan(sc[b, lens[b]:])), "entries past the context are left untouched"
+
+
+def test_indexer_bad_block_is_minus_inf():
+    m = lib()
+    wl = W.indexer_keys(DEV, seed=3, batch=2, n_heads=32, topk=64, ctx_lens=[640, 640])
+    bt = wl.block_table.clone()
+    bt[0, 2] = wl.num_blocks + 5
+    bt[1, 9] = -3
+    wl.block_table = bt
+    idx, sc = run_indexer(m, wl, 640)
+    assert np.all(np.isneginf(sc[0, 128:192])) and np.all(np.isneginf(sc[1, 576:640]))
+    assert np.all(np.isfinite(sc[0, :128])) and not np.isin(np.arange(128, 192), idx[0]).any()
+
+
+def test_chained_indexer_topk_decode_full_size():
+    """64 requests x 140,000 tokens: indexer + top-2048 on all requests vs the
+    oracle, then the NVFP4 decode of 4 requests on the selected rows."""
+    m = lib()
+    wl = W.indexer_keys(DEV, seed=0, batch=64, ctx=140_000, n_heads=32, topk=2048)
+    idx, sc = run_indexer(m, wl, 140_000)
+    ref = oracle_scores(wl, None, O.host_threads())
+    swaps = sum(check_request(idx[b], sc[b], ref[b], 2048) for b in range(64))
+    print(f"near-tie swaps against the float64 top-k over 64 requests: {swaps}")
+    # decode on the selected rows (16 MLA heads per request)
+    dec = W._decode_workload("chained", ("chained", 0), 64, 16, 2048, [140_000] * 64, DEV, 0.0,
+                             lambda b, c, g: torch.from_numpy(idx[b][idx[b] >= 0].astype(np.int64)).to(DEV))
+
+    def qa(lat, rope, slots, pool, nb, stride, fmt):
+        m.mla_kv_quantize_append(lat, rope, slots, pool, nb, 64, stride, fmt)
+
+    W.fill_pool(dec, O.FMT_NVFP4, qa)
+    lse = torch.empty((64, 16), dtype=torch.float32, device=DEV)
+    out, _ = m.mla_sparse_decode(dec.q_nope, dec.q_rope, dec.pools[0], dec.strides[0], dec.num_blocks,
+                                 dec.block_table, dec.context_lens, dec.topk_idx, dec.softmax_scale, lse=lse)
+    torch.cuda.synchronize()
+    out, lse = out.float().cpu().numpy(), lse.cpu().numpy()
+    for b in [0, 21, 42, 63]:
+        sel = torch.from_numpy(O.topk(ref[b], 2048).astype(np.int64)).to(DEV)
+        lat, rope = dec.request_rows(b, sel)
+        valid = np.ones(2048, bool)
+        r, rl = oracle_rows_decode(u16(dec.q_nope[b]), u16(dec.q_rope[b]), u16(lat), u16(rope), valid, 0,
+                                   dec.softmax_scale)
+        if set(idx[b].tolist()) == set(O.topk(ref[b], 2048).tolist()):
+            assert_decode_close(out[b], lse[b], r, rl, f"request {b}")

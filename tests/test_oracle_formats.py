@@ -262,7 +262,7 @@ def test_quantize_append_places_rows_by_slot_and_skips_negative_slots():
     rope = (rng.standard_normal((n, 64)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
     slots = np.array([0, 63, 64, 200, -1, 255, 130, -7, 5, 128], dtype=np.int64)
     pool = np.full(nb * stride, 0xCD, dtype=np.uint8)
-    O.kv_quantize_append(lat, rope, slots, pool, nb, bs, stride, O.FMT_NVFP4)
+    assert O.kv_quantize_append(lat, rope, slots, pool, nb, bs, stride, O.FMT_NVFP4) == 2
     touched = np.zeros(pool.size, dtype=bool)
     for i, s in enumerate(slots):
         if s < 0:
@@ -271,5 +271,7 @@ def test_quantize_append_places_rows_by_slot_and_skips_negative_slots():
         assert np.array_equal(pool[off:off + 352], O.quantize_row(lat[i], rope[i], O.FMT_NVFP4))
         touched[off:off + 352] = True
     assert np.all(pool[~touched] == 0xCD)
-    with pytest.raises(ValueError):
-        O.kv_quantize_append(lat[:1], rope[:1], np.array([nb * bs], np.int64), pool, nb, bs, stride, O.FMT_NVFP4)
+    before = pool.copy()
+    assert O.kv_quantize_append(lat[:2], rope[:2], np.array([nb * bs, -3], np.int64), pool, nb, bs, stride,
+                                O.FMT_NVFP4) == 2
+    assert np.array_equal(pool, before)  # slots past the pool are skipped, nothing is written
