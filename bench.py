@@ -44,11 +44,13 @@ FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--layers", type=int, default=0, help="distinct layer caches (0: enough to defeat L2)")
     p.add_argument("--no-extras", action="store_true", help="skip the append / indexer sub-measurements")
+    p.add_argument("--ctx", type=int, default=140_000,
+                   help="context length per request (smaller values only shrink the pools, for profiling)")
     return p.parse_args()
 
 
@@ -75,57 +77,96 @@ def decode_flops(batch, heads, topk):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    """SM clock and clock-event (throttle) reasons sampled while the timed
+    region runs: NVML through ctypes every ~1 ms (read-only queries), or
+    nvidia-smi every 200 ms if NVML cannot be loaded."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, gpu_index):
-        self.gpu = gpu_index
-        self.proc = None
-        self.lines = []
+    def __init__(self, pci_bus_id: str, smi_index: int = 0):
+        self.pci = pci_bus_id
+        self.smi_index = smi_index
+        self.samples = []  # (sm_mhz, reasons bitmask)
+        self.max_mhz = None
+        self.source = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._proc = None
+
+    def _nvml(self):
+        import ctypes as C
+        lib = C.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = C.c_void_p()
+        if lib.nvmlDeviceGetHandleByPciBusId_v2(self.pci.encode(), C.byref(h)) != 0:
+            raise OSError("no NVML handle for " + self.pci)
+        mx = C.c_uint(0)
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, C.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+        get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        clk, rs = C.c_uint(0), C.c_ulonglong(0)
+
+        def loop():
+            while not self._stop.is_set():
+                if lib.nvmlDeviceGetClockInfo(h, 1, C.byref(clk)) == 0 and get_reasons(h, C.byref(rs)) == 0:
+                    self.samples.append((float(clk.value), int(rs.value)))
+                time.sleep(0.001)
+        return loop
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
-                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.t = threading.Thread(target=self._read, daemon=True)
-            self.t.start()
-        except FileNotFoundError:
-            self.proc = None
+            loop = self._nvml()
+            self.source = "nvml"
+            self._thread = threading.Thread(target=loop, daemon=True)
+            self._thread.start()
+        except Exception:
+            self.source = "nvidia-smi"
+            fields = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                      "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                      "clocks_event_reasons.sw_power_cap")
+            try:
+                self._proc = subprocess.Popen(["nvidia-smi", "-i", str(self.smi_index), f"--query-gpu={fields}",
+                                               "--format=csv,noheader,nounits", "-lms", "200"],
+                                              stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self._thread = threading.Thread(target=self._read_smi, daemon=True)
+                self._thread.start()
+            except FileNotFoundError:
+                self._proc = None
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
+    def _read_smi(self):
+        bits = [0x8, 0x40, 0x20, 0x4]
+        for line in self._proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            try:
+                sm, self.max_mhz = float(parts[0]), float(parts[1])
+            except (ValueError, IndexError):
+                continue
+            mask = sum(b for b, v in zip(bits, parts[2:6]) if v.lower() == "active")
+            self.samples.append((sm, mask))
 
     def __exit__(self, *a):
-        if self.proc is not None:
-            self.proc.terminate()
+        self._stop.set()
+        if self._proc is not None:
+            self._proc.terminate()
             try:
-                self.proc.wait(timeout=5)
+                self._proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
-                self.proc.kill()
+                self._proc.kill()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx = float(parts[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        sm = [s for s, _ in self.samples]
+        mask = 0
+        for _, r in self.samples:
+            mask |= r
+        reasons = sorted(n for b, n in self.REASONS.items() if mask & b)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(sm), "source": self.source}
 
 
 # ------------------------------------------------------------------ reference arm (the oracle)
@@ -214,7 +255,7 @@ def main():
 
     layers = []
     for li in range(L):
-        wl = W.tp4_rank_decode(dev, seed=1000 * rank + li)
+        wl = W.tp4_rank_decode(dev, seed=1000 * rank + li, ctx=args.ctx)
         W.fill_pool(wl, 0, qa)
         W.fill_pool(wl, 1, qa)
         wl.out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=dev)
@@ -268,7 +309,9 @@ def main():
             ms = float(t)
         return ms
 
-    with ClockSampler(local) as clocks:
+    props = torch.cuda.get_device_properties(dev)
+    pci = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+    with ClockSampler(pci, local) as clocks:
         ms4 = timed(graphs[0], args.steps, args.warmup)
         ms8 = timed(graphs[1], args.steps, args.warmup)
     clk = clocks.summary()
@@ -334,12 +377,12 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms4, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": {"workload": "TP4 rank decode: 32 requests x 16 heads, 140,000-token contexts, top-2048 "
+        "config": {"workload": f"TP4 rank decode: 32 requests x 16 heads, {args.ctx:,}-token contexts, top-2048 "
                                "(70% prefix + 30% last 6,000), NVFP4 352-byte rows, block 64",
                    "layers_per_step": L, "l2": f"inputs larger than L2: {L} distinct layer caches, "
                                               f"{L * layer_bytes4 / 1e6:.0f} MB read per step vs "
                                               f"{l2 / 1e6:.0f} MB L2",
-                   "global_batch": B * world, "seq_len": 140_000, "parallelism": f"replicas x{world}"},
+                   "global_batch": B * world, "seq_len": args.ctx, "parallelism": f"replicas x{world}"},
         "per_layer_us": per_layer4 * 1e6,
         "hbm_gbs": ach4,
         "roofline": {"bound": "hbm" if layer_bytes4 / hbm / 1e9 >= fl / tf_burst / 1e12 else "tensor",

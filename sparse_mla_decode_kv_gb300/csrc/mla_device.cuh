@@ -27,9 +27,9 @@ constexpr int kIdxDim = 128;               // indexer key width (e4m3)
 // mla_api.cu whose address kernels receive as an argument).
 constexpr unsigned int kFaultDecodeWait = 1u;
 constexpr unsigned int kFaultIndexerWait = 2u;
-// Poll budget of a bounded wait (each poll backs off ~32-256 ns): on the
-// order of a second, far beyond any legitimate wait in these kernels.
-constexpr uint32_t kWaitPolls = 1u << 23;
+// Poll budget of the back-off phase of a bounded wait (each poll sleeps up to
+// ~1 us): seconds in total, far beyond any legitimate wait in these kernels.
+constexpr uint32_t kWaitPolls = 1u << 22;
 
 // ---- conversions -----------------------------------------------------------
 // Two e2m1 codes (low nibble -> low half) to two exact f16 values.
@@ -134,15 +134,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait for the phase with the given parity.  Returns false (after
-// setting `fault` in *fault_word) if it never completed.
+// Bounded wait for the phase with the given parity.  try_wait itself parks
+// the thread for a hardware-chosen interval, so the first polls spin; only
+// after kSpinPolls does the loop back off with nanosleep.  Returns false
+// (after setting `fault` in *fault_word) if the phase never completed.
+constexpr uint32_t kSpinPolls = 1u << 14;
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned int* fault_word,
                                                   unsigned int fault) {
-  if (mbar_try_wait(bar, parity)) return true;
-  uint32_t ns = 32;
+  for (uint32_t i = 0; i < kSpinPolls; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  uint32_t ns = 64;
   for (uint32_t i = 0; i < kWaitPolls; ++i) {
     __nanosleep(ns);
-    if (ns < 256) ns <<= 1;
+    if (ns < 1024) ns <<= 1;
     if (mbar_try_wait(bar, parity)) return true;
   }
   atomicOr(fault_word, fault);

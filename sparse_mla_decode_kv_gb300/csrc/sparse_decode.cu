@@ -52,6 +52,7 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStageRows = 32;
 constexpr int kStages = 4;
 constexpr int kHeadsPerCta = 16;
+constexpr int kMaxRows = 2048;  // rows of one CTA's slice (top-k <= 2048)
 constexpr int kRedPitch = 24;  // floats per token row of the partial-score exchange
 constexpr int kPPitch = 24;    // halfs per head row of P (48 bytes: ldmatrix conflict-free)
 constexpr float kLn2 = 0.6931471805599453f;
@@ -79,7 +80,8 @@ struct alignas(128) Smem {
   float alpha[kHeadsPerCta];
   float mfin[kHeadsPerCta];
   float lfin[kHeadsPerCta];
-  int32_t tok[kStages][kStageRows];
+  int32_t tok_all[kMaxRows];  // token of each row of the slice, -1 if masked
+  int32_t pb_all[kMaxRows];   // its physical block
   uint64_t full[kStages];
   uint64_t empty[kStages];
   int abort_flag;
@@ -107,10 +109,6 @@ struct DecodeArgs {
   unsigned int* fault_word;
 };
 
-__device__ __forceinline__ uint32_t dup_scale(uint32_t s_byte) {
-  // {S, S} as f16x2 from one e4m3 byte.
-  return e4m3x2_to_f16x2(s_byte | (s_byte << 8));
-}
 __device__ __forceinline__ uint32_t bf16pair_to_f16x2(uint32_t two) {
   return f32x2_to_f16x2_sat(bf16_bits_to_f32(two & 0xFFFFu), bf16_bits_to_f32(two >> 16));
 }
@@ -144,33 +142,50 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_decode_kernel(const Decode
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    const int32_t* topk_row = args.topk_idx + static_cast<int64_t>(b) * args.topk;
+    // Resolve the rows of the slice: the first kStages stages first (so their
+    // copies can start one index + one block-table round trip after launch),
+    // then the rest while those copies are in flight.  Loads are batched so
+    // that each lane has up to 8 independent requests outstanding.
+    const int32_t* topk_row = args.topk_idx + static_cast<int64_t>(b) * args.topk + row_begin;
     const int32_t* bt_row = args.block_table + static_cast<int64_t>(b) * args.max_blocks;
+    const int n_slots = n_stages * kStageRows;
+    auto resolve = [&](int lo, int hi) {
+      for (int base = lo; base < hi; base += 8 * 32) {
+        int t[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int j = base + u * 32 + lane;
+          t[u] = (j < hi && j < n_rows) ? __ldg(topk_row + j) : -1;
+        }
+        int pb[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const bool ok = t[u] >= 0 && t[u] < ctx && t[u] / kBlock < args.max_blocks;
+          pb[u] = ok ? __ldg(bt_row + t[u] / kBlock) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int j = base + u * 32 + lane;
+          const bool ok = pb[u] >= 0 && pb[u] < args.num_blocks;
+          if (j < hi) {
+            sm.tok_all[j] = ok ? t[u] : -1;
+            sm.pb_all[j] = ok ? pb[u] : -1;
+          }
+        }
+      }
+    };
+    const int first = min(n_slots, kStages * kStageRows);
+    resolve(0, first);
+    __syncwarp();
     int issued = 0;
     for (int it = 0; it < n_stages; ++it) {
       const int slot = it % kStages;
       const uint32_t round = it / kStages;
       const bool ok = mbar_wait_bounded(&sm.empty[slot], (round & 1u) ^ 1u, args.fault_word, kFaultDecodeWait);
       if (!__all_sync(0xFFFFFFFFu, ok)) break;  // warp-uniform decision
-      const int j = row_begin + it * kStageRows + lane;
-      int t = -1;
-      const uint8_t* src = nullptr;
-      if (j < row_end) {
-        const int t0 = __ldg(topk_row + j);
-        if (t0 >= 0 && t0 < ctx) {
-          const int lb = t0 / kBlock;
-          if (lb < args.max_blocks) {
-            const int pb = __ldg(bt_row + lb);
-            if (pb >= 0 && pb < args.num_blocks) {
-              t = t0;
-              src = args.pool + static_cast<int64_t>(pb) * args.block_stride +
-                    static_cast<int64_t>(t0 % kBlock) * F::kRowBytes;
-            }
-          }
-        }
-      }
+      const int j = it * kStageRows + lane;
+      const int t = sm.tok_all[j];
       uint8_t* dst = sm.rows[slot][lane];
-      sm.tok[slot][lane] = t;
       if (t < 0) {
 #pragma unroll
         for (int i = 0; i < F::kRowBytes / 16; ++i) reinterpret_cast<uint4*>(dst)[i] = make_uint4(0, 0, 0, 0);
@@ -179,8 +194,16 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_decode_kernel(const Decode
       __syncwarp();
       if (lane == 0) mbar_arrive_expect_tx(&sm.full[slot], __popc(valid) * F::kRowBytes);
       __syncwarp();
-      if (t >= 0) bulk_g2s(dst, src, F::kRowBytes, &sm.full[slot]);
+      if (t >= 0) {
+        const uint8_t* src = args.pool + static_cast<int64_t>(sm.pb_all[j]) * args.block_stride +
+                             static_cast<int64_t>(t % kBlock) * F::kRowBytes;
+        bulk_g2s(dst, src, F::kRowBytes, &sm.full[slot]);
+      }
       issued = it + 1;
+      if (it == min(n_stages, kStages) - 1 && n_slots > first) {
+        resolve(first, n_slots);  // the remaining rows, behind the first copies
+        __syncwarp();
+      }
     }
     // Never leave with copies in flight: wait for the last stages issued.
     for (int it = max(0, issued - kStages); it < issued; ++it)
@@ -241,14 +264,26 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_decode_kernel(const Decode
       const uint8_t* row1 = row0 + 8 * F::kPitch;
       uint32_t a[9][4];
       if constexpr (FMT == 0) {
+        // Scales of groups 8w + 2q + (c>>1), q = 0..3: one 8-byte load per row,
+        // two byte permutes, two conversions, then {S, S} duplicates.
+        const uint32_t sel = (c >> 1) ? 0x3131u : 0x2020u;
+        const uint2 sw0 = *reinterpret_cast<const uint2*>(row0 + kScaleOff + 8 * w);
+        const uint2 sw1 = *reinterpret_cast<const uint2*>(row1 + kScaleOff + 8 * w);
+        const uint32_t s0_01 = e4m3x2_to_f16x2(__byte_perm(sw0.x, 0, sel));
+        const uint32_t s0_23 = e4m3x2_to_f16x2(__byte_perm(sw0.y, 0, sel));
+        const uint32_t s1_01 = e4m3x2_to_f16x2(__byte_perm(sw1.x, 0, sel));
+        const uint32_t s1_23 = e4m3x2_to_f16x2(__byte_perm(sw1.y, 0, sel));
+        const uint32_t sc0[4] = {__byte_perm(s0_01, 0, 0x1010), __byte_perm(s0_01, 0, 0x3232),
+                                 __byte_perm(s0_23, 0, 0x1010), __byte_perm(s0_23, 0, 0x3232)};
+        const uint32_t sc1[4] = {__byte_perm(s1_01, 0, 0x1010), __byte_perm(s1_01, 0, 0x3232),
+                                 __byte_perm(s1_23, 0, 0x1010), __byte_perm(s1_23, 0, 0x3232)};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int off = 64 * w + 16 * q + 4 * c;
           const uint32_t w0 = *reinterpret_cast<const uint32_t*>(row0 + off);
           const uint32_t w1 = *reinterpret_cast<const uint32_t*>(row1 + off);
-          const int soff = kScaleOff + 8 * w + 2 * q + (c >> 1);
-          const uint32_t s0 = dup_scale(row0[soff]);
-          const uint32_t s1 = dup_scale(row1[soff]);
+          const uint32_t s0 = sc0[q];
+          const uint32_t s1 = sc1[q];
           a[2 * q][0] = hmul2(e2m1x2_to_f16x2(w0 & 0xFFu), s0);
           a[2 * q][1] = hmul2(e2m1x2_to_f16x2(w1 & 0xFFu), s1);
           a[2 * q][2] = hmul2(e2m1x2_to_f16x2((w0 >> 8) & 0xFFu), s0);
@@ -286,11 +321,20 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_decode_kernel(const Decode
 
       // Partial scores over this warp's 144 dims: S^T [16 tokens x 16 heads].
       float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      float sodd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // second chain: shorter dependency
 #pragma unroll
-      for (int ks = 0; ks < 9; ++ks) {
+      for (int ks = 0; ks < 9; ks += 2) {
         mma_f16(sacc[0], a[ks], bq[ks][0][0], bq[ks][0][1]);
         mma_f16(sacc[1], a[ks], bq[ks][1][0], bq[ks][1][1]);
+        if (ks + 1 < 9) {
+          mma_f16(sodd[0], a[ks + 1], bq[ks + 1][0][0], bq[ks + 1][0][1]);
+          mma_f16(sodd[1], a[ks + 1], bq[ks + 1][1][0], bq[ks + 1][1][1]);
+        }
       }
+#pragma unroll
+      for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[n][e] += sodd[n][e];
 #pragma unroll
       for (int n = 0; n < 2; ++n) {
         *reinterpret_cast<float2*>(&sm.red[w][g][8 * n + 2 * c]) = make_float2(sacc[n][0], sacc[n][1]);
@@ -311,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_decode_kernel(const Decode
           s.x += v.x;
           s.y += v.y;
         }
-        const bool valid = sm.tok[slot][16 * mt + tloc] >= 0;
+        const bool valid = sm.tok_all[it * kStageRows + 16 * mt + tloc] >= 0;
         float z[2] = {valid ? s.x * args.scale_log2 : -INFINITY, valid ? s.y * args.scale_log2 : -INFINITY};
         __half ph[2];
 #pragma unroll
@@ -425,48 +469,36 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_decode_kernel(const Decode
 }
 
 // Combine `splits` normalised partial outputs with their base-2 LSEs:
-// LSE = log2 sum_s 2^lse_s, out = sum_s 2^(lse_s - LSE) * O_s.  One warp per
-// (request, head); lane l handles dims [16l, 16l+16).
+// LSE = log2 sum_s 2^lse_s, out = sum_s 2^(lse_s - LSE) * O_s.  One CTA per
+// (request, head); thread i handles dims [4i, 4i+4).
 __global__ void __launch_bounds__(128) splitk_merge_kernel(const float* __restrict__ part_o,
-                                                           const float* __restrict__ part_lse, int64_t n_bh,
-                                                           int splits, uint16_t* __restrict__ out,
-                                                           float* __restrict__ lse) {
-  const int64_t bh = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (bh >= n_bh) return;
+                                                           const float* __restrict__ part_lse, int splits,
+                                                           uint16_t* __restrict__ out, float* __restrict__ lse) {
+  const int64_t bh = blockIdx.x;
+  const int t = threadIdx.x;
   const float* pl = part_lse + bh * splits;
   float mx = -INFINITY;
   for (int s = 0; s < splits; ++s) mx = fmaxf(mx, __ldg(pl + s));
-  float acc[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
   if (mx != -INFINITY) {
+    const float4* src = reinterpret_cast<const float4*>(part_o + bh * splits * kLatent) + t;
     for (int s = 0; s < splits; ++s) {
       const float ws = ex2(__ldg(pl + s) - mx);
+      const float4 v = __ldg(src + s * (kLatent / 4));
       wsum += ws;
-      const float4* src = reinterpret_cast<const float4*>(part_o + (bh * splits + s) * kLatent + 16 * lane);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float4 v = __ldg(src + i);
-        acc[4 * i] += ws * v.x;
-        acc[4 * i + 1] += ws * v.y;
-        acc[4 * i + 2] += ws * v.z;
-        acc[4 * i + 3] += ws * v.w;
-      }
+      acc.x += ws * v.x;
+      acc.y += ws * v.y;
+      acc.z += ws * v.z;
+      acc.w += ws * v.w;
     }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  uint32_t r[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    __nv_bfloat162 x = __floats2bfloat162_rn(acc[2 * i] * inv, acc[2 * i + 1] * inv);
-    r[i] = *reinterpret_cast<uint32_t*>(&x);
-  }
-  uint4* dst = reinterpret_cast<uint4*>(out + bh * kLatent + 16 * lane);
-  dst[0] = make_uint4(r[0], r[1], r[2], r[3]);
-  dst[1] = make_uint4(r[4], r[5], r[6], r[7]);
-  if (lse != nullptr && lane == 0) lse[bh] = wsum > 0.f ? (mx + lg2(wsum)) * kLn2 : -INFINITY;
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2*>(out + bh * kLatent + 4 * t) =
+      make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+  if (lse != nullptr && t == 0) lse[bh] = wsum > 0.f ? (mx + lg2(wsum)) * kLn2 : -INFINITY;
 }
 
 template <int FMT>
@@ -547,8 +579,7 @@ cudaError_t launch_sparse_decode(int fmt, const uint16_t* q_nope, const uint16_t
   cudaError_t e = fmt == 0 ? launch_fmt<0>(a, batch, stream) : launch_fmt<1>(a, batch, stream);
   if (e != cudaSuccess || plan.splits == 1) return e;
   const int64_t n_bh = static_cast<int64_t>(batch) * num_heads;
-  splitk_merge_kernel<<<static_cast<unsigned>((n_bh + 3) / 4), 128, 0, stream>>>(a.part_o, a.part_lse, n_bh,
-                                                                                 plan.splits, out, lse);
+  splitk_merge_kernel<<<static_cast<unsigned>(n_bh), 128, 0, stream>>>(a.part_o, a.part_lse, plan.splits, out, lse);
   return cudaGetLastError();
 }
 
