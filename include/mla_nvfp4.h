@@ -151,6 +151,37 @@ mla_status_t mla_sparse_decode(const uint16_t* q_nope, const uint16_t* q_rope, c
                                uint16_t* out, float* lse, void* workspace, size_t workspace_bytes,
                                mla_stream_t stream);
 
+/*
+ * Allocation-free variant of mla_sparse_decode (NVFP4 cache).  The pages
+ * describe no such entry point; it exists for callers that cannot allocate
+ * device memory when they call the decode: a serving process that reserves
+ * its whole device-memory budget at start-up and may not grow it afterwards,
+ * or a plain C host that embeds this library without a device allocator of
+ * its own.  Those callers still own and pass every input and output buffer;
+ * only the split-K scratch moves into the library.
+ *
+ *  - Arguments, results and errors are those of mla_sparse_decode, without
+ *    the workspace pair.
+ *  - The scratch is one file-scope device array of
+ *    MLA_SPARSE_DECODE_NOALLOC_SCRATCH_BYTES (16 MiB) that every GPU which
+ *    loads the library holds until the process exits.  A call whose
+ *    mla_sparse_decode_workspace_size(batch, num_heads, topk) exceeds it
+ *    returns MLA_ERR_WORKSPACE_TOO_SMALL and launches nothing.
+ *  - The first call on a device looks up that device's address of the array
+ *    (with the device current) and caches it; make that first call before any
+ *    stream capture.  The call itself never calls cudaMalloc or cudaFree.
+ *  - Every call on a device shares the same array, which keeps whatever the
+ *    last call left there (nothing in it needs to start at zero).  Calls that
+ *    overlap on the GPU -- on different streams, or from different host
+ *    threads -- race on it and must be serialised by the caller.
+ */
+#define MLA_SPARSE_DECODE_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+mla_status_t mla_sparse_decode_noalloc(const uint16_t* q_nope, const uint16_t* q_rope, const void* kv_pool,
+                                       int64_t kv_block_stride, int64_t num_blocks, const int32_t* block_table,
+                                       int max_blocks_per_req, const int32_t* context_lens, const int32_t* topk_idx,
+                                       int batch, int num_heads, int block_size, int topk, float softmax_scale,
+                                       uint16_t* out, float* lse, mla_stream_t stream);
+
 /* The same decode over the 576-byte FP8 cache: c_t and r_t are the e4m3
  * bytes themselves.  This is the in-library comparison path ("Prime
  * Inference", figure "staged vs native decode": FP8 attention on a real FP8

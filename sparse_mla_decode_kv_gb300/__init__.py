@@ -18,7 +18,7 @@ __all__ = [
     "MlaError", "MLA_KV_NVFP4", "MLA_KV_FP8", "library_path", "load",
     "mla_kv_row_bytes", "mla_status_string", "mla_last_cuda_error", "mla_device_fault",
     "mla_kv_quantize_append", "mla_sparse_decode_workspace_size", "mla_sparse_decode",
-    "mla_sparse_decode_fp8", "mla_topk_workspace_size", "mla_topk",
+    "mla_sparse_decode_fp8", "mla_sparse_decode_noalloc", "mla_topk_workspace_size", "mla_topk",
     "mla_indexer_topk_workspace_size", "mla_indexer_topk",
 ]
 
@@ -44,6 +44,8 @@ SIGNATURES = {
                                  _P, _SZ, _P]),
     "mla_sparse_decode_fp8": (_I32, [_P, _P, _P, _I64, _I64, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _F32, _P,
                                      _P, _P, _SZ, _P]),
+    "mla_sparse_decode_noalloc": (_I32, [_P, _P, _P, _I64, _I64, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _F32, _P,
+                                         _P, _P]),
     "mla_topk_workspace_size": (_SZ, [_I32, _I32, _I32]),
     "mla_topk": (_I32, [_P, _I64, _P, _I32, _I32, _I32, _P, _P, _SZ, _P]),
     "mla_indexer_topk_workspace_size": (_SZ, [_I32, _I32, _I32]),
@@ -195,6 +197,27 @@ def mla_sparse_decode_fp8(q_nope, q_rope, kv_pool, kv_block_stride, num_blocks, 
     """FP8 (576-byte) cache.  Returns (out bf16 [B,H,512], lse or None)."""
     return _decode("mla_sparse_decode_fp8", q_nope, q_rope, kv_pool, kv_block_stride, num_blocks, block_table,
                    context_lens, topk_idx, softmax_scale, block_size, out, lse, workspace, stream)
+
+
+def mla_sparse_decode_noalloc(q_nope, q_rope, kv_pool, kv_block_stride, num_blocks, block_table, context_lens,
+                              topk_idx, softmax_scale, block_size=64, out=None, lse=None, stream=None):
+    """NVFP4 decode whose split-K scratch is the library's own fixed device
+    array (for callers that cannot allocate); same results as
+    mla_sparse_decode.  Returns (out bf16 [B,H,512], lse or None)."""
+    q_nope = _bits(q_nope, "q_nope")
+    q_rope = _bits(q_rope, "q_rope")
+    block_table = _contig(block_table, torch.int32, "block_table")
+    context_lens = _contig(context_lens, torch.int32, "context_lens")
+    topk_idx = _contig(topk_idx, torch.int32, "topk_idx")
+    batch, heads = q_nope.shape[0], q_nope.shape[1]
+    if out is None:
+        out = torch.empty((batch, heads, 512), dtype=torch.bfloat16, device=q_nope.device)
+    _check("mla_sparse_decode_noalloc",
+           load().mla_sparse_decode_noalloc(_ptr(q_nope), _ptr(q_rope), _ptr(kv_pool), kv_block_stride, num_blocks,
+                                            _ptr(block_table), block_table.shape[1], _ptr(context_lens),
+                                            _ptr(topk_idx), batch, heads, block_size, topk_idx.shape[1],
+                                            float(softmax_scale), _ptr(out), _ptr(lse), _stream(stream)))
+    return out, lse
 
 
 # --------------------------------------------------------------------- top-k and indexer
