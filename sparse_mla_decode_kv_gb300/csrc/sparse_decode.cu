@@ -48,13 +48,17 @@ namespace mla {
 namespace {
 
 constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStageRows = 32;
-constexpr int kStages = 4;
+constexpr int kThreads = kConsumerWarps * 32;  // all warps consume; warp 0 also refills stages
+constexpr int kStageRows = 32;  // one stage = one phase = two 16-row m-tiles
 constexpr int kHeadsPerCta = 16;
 constexpr int kMaxRows = 2048;  // rows of one CTA's slice (top-k <= 2048)
 constexpr int kRedPitch = 24;  // floats per token row of the partial-score exchange
-constexpr int kPPitch = 24;    // halfs per head row of P (48 bytes: ldmatrix conflict-free)
+constexpr int kPPitch = 40;    // halfs per head row of P (80 bytes: ldmatrix conflict-free)
+constexpr int kKSteps = 9;     // k-steps of 16 dims per consumer warp (128 latent + 16 rope)
+// Lazy softmax maximum: scores are exponentiated against a reference maximum
+// that is raised only when a score exceeds it by more than kLazy (base 2), so
+// P stays <= 2^kLazy (fine in f16) and the common path needs no reduction.
+constexpr float kLazy = 8.f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 template <int FMT>
@@ -64,26 +68,29 @@ struct Fmt<0> {
   static constexpr int kRowBytes = kRowNvfp4;
   static constexpr int kPitch = kRowNvfp4 + 16;  // 368: conflict-free fragment loads
   static constexpr int kRopeOff = kRopeOffNvfp4;
+  static constexpr int kStages = 4;
 };
 template <>
 struct Fmt<1> {
   static constexpr int kRowBytes = kRowFp8;
   static constexpr int kPitch = kRowFp8 + 16;  // 592
   static constexpr int kRopeOff = kRopeOffFp8;
+  static constexpr int kStages = 3;  // two CTAs per SM still fit
 };
 
 template <int FMT>
 struct alignas(128) Smem {
-  uint8_t rows[kStages][kStageRows][Fmt<FMT>::kPitch];
-  float red[kConsumerWarps][16][kRedPitch];
+  uint8_t rows[Fmt<FMT>::kStages][kStageRows][Fmt<FMT>::kPitch];
+  uint4 qfrag[kConsumerWarps][kKSteps][32];  // query B fragments, fragment order
+  float red[kConsumerWarps][kStageRows][kRedPitch];
   __half pbuf[kHeadsPerCta][kPPitch];
   float alpha[kHeadsPerCta];
+  int rescale[kConsumerWarps];
   float mfin[kHeadsPerCta];
   float lfin[kHeadsPerCta];
+  int64_t row_off[kMaxRows];  // byte offset of each row of the slice in the pool
   int32_t tok_all[kMaxRows];  // token of each row of the slice, -1 if masked
-  int32_t pb_all[kMaxRows];   // its physical block
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[Fmt<FMT>::kStages];
   int abort_flag;
 };
 
@@ -114,8 +121,9 @@ __device__ __forceinline__ uint32_t bf16pair_to_f16x2(uint32_t two) {
 }
 
 template <int FMT>
-__global__ void __launch_bounds__(kThreads, 2) sparse_decode_kernel(const DecodeArgs args) {
+__global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(const DecodeArgs args) {
   using F = Fmt<FMT>;
+  constexpr int kStages = F::kStages;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem<FMT>& sm = *reinterpret_cast<Smem<FMT>*>(smem_raw);
 
@@ -130,112 +138,99 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_decode_kernel(const Decode
   const int n_stages = (n_rows + kStageRows - 1) / kStageRows;
   const int ctx = __ldg(args.ctx_lens + b);
 
+  // The split merge (launched as a programmatic dependent) may start its
+  // launch now; it waits for this whole grid before reading any partial.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], kConsumerWarps);
-    }
+    for (int s = 0; s < kStages; ++s) mbar_init(&sm.full[s], kThreads);
     sm.abort_flag = 0;
     fence_mbar_init();
   }
-  __syncthreads();
-
-  if (warp == kConsumerWarps) {
-    // ------------------------------------------------------------ producer
-    // Resolve the rows of the slice: the first kStages stages first (so their
-    // copies can start one index + one block-table round trip after launch),
-    // then the rest while those copies are in flight.  Loads are batched so
-    // that each lane has up to 8 independent requests outstanding.
-    const int32_t* topk_row = args.topk_idx + static_cast<int64_t>(b) * args.topk + row_begin;
-    const int32_t* bt_row = args.block_table + static_cast<int64_t>(b) * args.max_blocks;
-    const int n_slots = n_stages * kStageRows;
-    auto resolve = [&](int lo, int hi) {
-      for (int base = lo; base < hi; base += 8 * 32) {
-        int t[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int j = base + u * 32 + lane;
-          t[u] = (j < hi && j < n_rows) ? __ldg(topk_row + j) : -1;
-        }
-        int pb[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const bool ok = t[u] >= 0 && t[u] < ctx && t[u] / kBlock < args.max_blocks;
-          pb[u] = ok ? __ldg(bt_row + t[u] / kBlock) : -1;
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int j = base + u * 32 + lane;
-          const bool ok = pb[u] >= 0 && pb[u] < args.num_blocks;
-          if (j < hi) {
-            sm.tok_all[j] = ok ? t[u] : -1;
-            sm.pb_all[j] = ok ? pb[u] : -1;
-          }
-        }
-      }
-    };
-    const int first = min(n_slots, kStages * kStageRows);
-    resolve(0, first);
-    __syncwarp();
-    int issued = 0;
-    for (int it = 0; it < n_stages; ++it) {
-      const int slot = it % kStages;
-      const uint32_t round = it / kStages;
-      const bool ok = mbar_wait_bounded(&sm.empty[slot], (round & 1u) ^ 1u, args.fault_word, kFaultDecodeWait);
-      if (!__all_sync(0xFFFFFFFFu, ok)) break;  // warp-uniform decision
-      const int j = it * kStageRows + lane;
-      const int t = sm.tok_all[j];
-      uint8_t* dst = sm.rows[slot][lane];
-      if (t < 0) {
-#pragma unroll
-        for (int i = 0; i < F::kRowBytes / 16; ++i) reinterpret_cast<uint4*>(dst)[i] = make_uint4(0, 0, 0, 0);
-      }
-      const uint32_t valid = __ballot_sync(0xFFFFFFFFu, t >= 0);
-      __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(&sm.full[slot], __popc(valid) * F::kRowBytes);
-      __syncwarp();
-      if (t >= 0) {
-        const uint8_t* src = args.pool + static_cast<int64_t>(sm.pb_all[j]) * args.block_stride +
-                             static_cast<int64_t>(t % kBlock) * F::kRowBytes;
-        bulk_g2s(dst, src, F::kRowBytes, &sm.full[slot]);
-      }
-      issued = it + 1;
-      if (it == min(n_stages, kStages) - 1 && n_slots > first) {
-        resolve(first, n_slots);  // the remaining rows, behind the first copies
-        __syncwarp();
-      }
-    }
-    // Never leave with copies in flight: wait for the last stages issued.
-    for (int it = max(0, issued - kStages); it < issued; ++it)
-      mbar_wait_bounded(&sm.full[it % kStages], (static_cast<uint32_t>(it / kStages)) & 1u, args.fault_word, kFaultDecodeWait);
-    return;
-  }
-
-  // -------------------------------------------------------------- consumers
   const int g = lane >> 2;
   const int c = lane & 3;
   const int w = warp;
 
-  // Absorbed query as B fragments (K = this warp's 144 dims, N = 16 heads).
-  uint32_t bq[9][2][2];
+  // The absorbed query of this warp's dims, loaded first: it does not depend
+  // on the row resolution below, so its latency overlaps it.
+  const int h0 = hg * kHeadsPerCta + g;
+  const uint16_t* qn0 = args.q_nope + (static_cast<int64_t>(b) * args.num_heads + h0) * kLatent + 128 * w + 8 * c;
+  const uint16_t* qr0 = args.q_rope + (static_cast<int64_t>(b) * args.num_heads + h0) * kRope + 16 * w + 4 * c;
+  uint4 qv0[4], qv1[4];
 #pragma unroll
-  for (int n = 0; n < 2; ++n) {
-    const int h = hg * kHeadsPerCta + 8 * n + g;
-    const uint16_t* qn = args.q_nope + (static_cast<int64_t>(b) * args.num_heads + h) * kLatent;
-    const uint16_t* qr = args.q_rope + (static_cast<int64_t>(b) * args.num_heads + h) * kRope;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(qn + 128 * w + 32 * q + 8 * c));
-      bq[2 * q][n][0] = bf16pair_to_f16x2(v.x);
-      bq[2 * q][n][1] = bf16pair_to_f16x2(v.y);
-      bq[2 * q + 1][n][0] = bf16pair_to_f16x2(v.z);
-      bq[2 * q + 1][n][1] = bf16pair_to_f16x2(v.w);
-    }
-    const uint2 r = __ldg(reinterpret_cast<const uint2*>(qr + 16 * w + 4 * c));
-    bq[8][n][0] = bf16pair_to_f16x2(r.x);
-    bq[8][n][1] = bf16pair_to_f16x2(r.y);
+  for (int q = 0; q < 4; ++q) {
+    qv0[q] = __ldg(reinterpret_cast<const uint4*>(qn0 + 32 * q));
+    qv1[q] = __ldg(reinterpret_cast<const uint4*>(qn0 + 8 * kLatent + 32 * q));  // head h0 + 8
   }
+  const uint2 qr_0 = __ldg(reinterpret_cast<const uint2*>(qr0));
+  const uint2 qr_1 = __ldg(reinterpret_cast<const uint2*>(qr0 + 8 * kRope));
 
+  // ---------------------------------------------------------------- rows
+  // Resolve every row of the slice (top-k index, then block table) with all
+  // threads, in batches of independent loads: two round trips in total.
+  const int32_t* topk_row = args.topk_idx + static_cast<int64_t>(b) * args.topk + row_begin;
+  const int32_t* bt_row = args.block_table + static_cast<int64_t>(b) * args.max_blocks;
+  const int n_slots = n_stages * kStageRows;
+  for (int base = 0; base < n_slots; base += 4 * kThreads) {
+    int t[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j = base + u * kThreads + threadIdx.x;
+      t[u] = (j < n_rows) ? __ldg(topk_row + j) : -1;
+    }
+    int pb[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const bool ok = t[u] >= 0 && t[u] < ctx && t[u] / kBlock < args.max_blocks;
+      pb[u] = ok ? __ldg(bt_row + t[u] / kBlock) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j = base + u * kThreads + threadIdx.x;
+      const bool ok = pb[u] >= 0 && pb[u] < args.num_blocks;
+      if (j < n_slots) {
+        sm.tok_all[j] = ok ? t[u] : -1;
+        sm.row_off[j] = ok ? static_cast<int64_t>(pb[u]) * args.block_stride +
+                                 static_cast<int64_t>(t[u] % kBlock) * F::kRowBytes
+                           : -1;
+      }
+    }
+  }
+  __syncthreads();  // barrier init and the resolved rows are visible
+
+  // All threads fill stage `it` into its ring slot with 16-byte cp.async
+  // (masked rows zero-filled), then arrive on full[slot] when theirs land.
+  constexpr int kChunks = F::kRowBytes / 16;
+  auto fill_stage = [&](int it) {
+    const int slot = it % kStages;
+    for (int i = threadIdx.x; i < kStageRows * kChunks; i += kThreads) {
+      const int r = i / kChunks, k = i - (i / kChunks) * kChunks;
+      const int64_t off = sm.row_off[it * kStageRows + r];
+      const uint8_t* src = args.pool + (off >= 0 ? off : 0) + 16 * k;
+      cp_async16(sm.rows[slot][r] + 16 * k, src, off >= 0 ? 16u : 0u);
+    }
+    cp_async_arrive(&sm.full[slot]);
+  };
+  // Only two stages up front: the copies of every CTA start together, and a
+  // deeper initial burst would only delay the first stage behind the others.
+  // The rest of the ring is filled at the following stage boundaries.
+  constexpr int kInitialStages = 2;
+  int next_fill = 0;
+  for (; next_fill < min(n_stages, kInitialStages); ++next_fill) fill_stage(next_fill);
+
+  // Stage the query as B fragments (K = this warp's 144 dims in the permuted
+  // order, N = 16 heads) in fragment order: one 16-byte load per k-step.
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    sm.qfrag[w][2 * q][lane] = make_uint4(bf16pair_to_f16x2(qv0[q].x), bf16pair_to_f16x2(qv0[q].y),
+                                          bf16pair_to_f16x2(qv1[q].x), bf16pair_to_f16x2(qv1[q].y));
+    sm.qfrag[w][2 * q + 1][lane] = make_uint4(bf16pair_to_f16x2(qv0[q].z), bf16pair_to_f16x2(qv0[q].w),
+                                              bf16pair_to_f16x2(qv1[q].z), bf16pair_to_f16x2(qv1[q].w));
+  }
+  sm.qfrag[w][8][lane] = make_uint4(bf16pair_to_f16x2(qr_0.x), bf16pair_to_f16x2(qr_0.y),
+                                    bf16pair_to_f16x2(qr_1.x), bf16pair_to_f16x2(qr_1.y));
+  __syncwarp();
+
+  // -------------------------------------------------------------- consumers
   float o[8][2][4];
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks)
@@ -244,12 +239,12 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_decode_kernel(const Decode
 #pragma unroll
       for (int e = 0; e < 4; ++e) o[ks][be][e] = 0.f;
 
-  // Online-softmax state of the two heads this lane tracks as head owner.
-  const int hown = 4 * w + 2 * (lane & 1);
-  const int tloc = lane >> 1;
-  float m_run[2] = {-INFINITY, -INFINITY};
-  float l_run[2] = {0.f, 0.f};
+  // Softmax state: as head owner, warp w tracks heads 4w..4w+3 and lane =
+  // token of the stage; m_ref is warp-uniform, l_run is this lane's share.
+  float m_ref[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  float l_run[4] = {0.f, 0.f, 0.f, 0.f};
   bool aborted = false;
+  int abort_it = 0;
 
   for (int it = 0; it < n_stages && !aborted; ++it) {
     const int slot = it % kStages;
@@ -258,14 +253,15 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_decode_kernel(const Decode
     if (!__all_sync(0xFFFFFFFFu, ok) && lane == 0) sm.abort_flag = 1;  // all warps leave after the next barrier
     const uint8_t* base = sm.rows[slot][0];
 
-#pragma unroll 1
+    // ---- unpack this warp's dims of both m-tiles straight into A fragments
+    uint32_t a[2][kKSteps][4];
+#pragma unroll
     for (int mt = 0; mt < 2; ++mt) {
       const uint8_t* row0 = base + (16 * mt + g) * F::kPitch;
       const uint8_t* row1 = row0 + 8 * F::kPitch;
-      uint32_t a[9][4];
       if constexpr (FMT == 0) {
         // Scales of groups 8w + 2q + (c>>1), q = 0..3: one 8-byte load per row,
-        // two byte permutes, two conversions, then {S, S} duplicates.
+        // a byte permute and a conversion per pair, then {S, S} duplicates.
         const uint32_t sel = (c >> 1) ? 0x3131u : 0x2020u;
         const uint2 sw0 = *reinterpret_cast<const uint2*>(row0 + kScaleOff + 8 * w);
         const uint2 sw1 = *reinterpret_cast<const uint2*>(row1 + kScaleOff + 8 * w);
@@ -273,25 +269,21 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_decode_kernel(const Decode
         const uint32_t s0_23 = e4m3x2_to_f16x2(__byte_perm(sw0.y, 0, sel));
         const uint32_t s1_01 = e4m3x2_to_f16x2(__byte_perm(sw1.x, 0, sel));
         const uint32_t s1_23 = e4m3x2_to_f16x2(__byte_perm(sw1.y, 0, sel));
-        const uint32_t sc0[4] = {__byte_perm(s0_01, 0, 0x1010), __byte_perm(s0_01, 0, 0x3232),
-                                 __byte_perm(s0_23, 0, 0x1010), __byte_perm(s0_23, 0, 0x3232)};
-        const uint32_t sc1[4] = {__byte_perm(s1_01, 0, 0x1010), __byte_perm(s1_01, 0, 0x3232),
-                                 __byte_perm(s1_23, 0, 0x1010), __byte_perm(s1_23, 0, 0x3232)};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int off = 64 * w + 16 * q + 4 * c;
           const uint32_t w0 = *reinterpret_cast<const uint32_t*>(row0 + off);
           const uint32_t w1 = *reinterpret_cast<const uint32_t*>(row1 + off);
-          const uint32_t s0 = sc0[q];
-          const uint32_t s1 = sc1[q];
-          a[2 * q][0] = hmul2(e2m1x2_to_f16x2(w0 & 0xFFu), s0);
-          a[2 * q][1] = hmul2(e2m1x2_to_f16x2(w1 & 0xFFu), s1);
-          a[2 * q][2] = hmul2(e2m1x2_to_f16x2((w0 >> 8) & 0xFFu), s0);
-          a[2 * q][3] = hmul2(e2m1x2_to_f16x2((w1 >> 8) & 0xFFu), s1);
-          a[2 * q + 1][0] = hmul2(e2m1x2_to_f16x2((w0 >> 16) & 0xFFu), s0);
-          a[2 * q + 1][1] = hmul2(e2m1x2_to_f16x2((w1 >> 16) & 0xFFu), s1);
-          a[2 * q + 1][2] = hmul2(e2m1x2_to_f16x2(w0 >> 24), s0);
-          a[2 * q + 1][3] = hmul2(e2m1x2_to_f16x2(w1 >> 24), s1);
+          const uint32_t s0 = __byte_perm(q < 2 ? s0_01 : s0_23, 0, (q & 1) ? 0x3232 : 0x1010);
+          const uint32_t s1 = __byte_perm(q < 2 ? s1_01 : s1_23, 0, (q & 1) ? 0x3232 : 0x1010);
+          a[mt][2 * q][0] = hmul2(e2m1x2_to_f16x2(w0 & 0xFFu), s0);
+          a[mt][2 * q][1] = hmul2(e2m1x2_to_f16x2(w1 & 0xFFu), s1);
+          a[mt][2 * q][2] = hmul2(e2m1x2_to_f16x2((w0 >> 8) & 0xFFu), s0);
+          a[mt][2 * q][3] = hmul2(e2m1x2_to_f16x2((w1 >> 8) & 0xFFu), s1);
+          a[mt][2 * q + 1][0] = hmul2(e2m1x2_to_f16x2((w0 >> 16) & 0xFFu), s0);
+          a[mt][2 * q + 1][1] = hmul2(e2m1x2_to_f16x2((w1 >> 16) & 0xFFu), s1);
+          a[mt][2 * q + 1][2] = hmul2(e2m1x2_to_f16x2(w0 >> 24), s0);
+          a[mt][2 * q + 1][3] = hmul2(e2m1x2_to_f16x2(w1 >> 24), s1);
         }
       } else {
 #pragma unroll
@@ -299,124 +291,156 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_decode_kernel(const Decode
           const int off = 128 * w + 32 * q + 8 * c;
           const uint2 v0 = *reinterpret_cast<const uint2*>(row0 + off);
           const uint2 v1 = *reinterpret_cast<const uint2*>(row1 + off);
-          a[2 * q][0] = e4m3x2_to_f16x2(v0.x);
-          a[2 * q][1] = e4m3x2_to_f16x2(v1.x);
-          a[2 * q][2] = e4m3x2_to_f16x2(v0.x >> 16);
-          a[2 * q][3] = e4m3x2_to_f16x2(v1.x >> 16);
-          a[2 * q + 1][0] = e4m3x2_to_f16x2(v0.y);
-          a[2 * q + 1][1] = e4m3x2_to_f16x2(v1.y);
-          a[2 * q + 1][2] = e4m3x2_to_f16x2(v0.y >> 16);
-          a[2 * q + 1][3] = e4m3x2_to_f16x2(v1.y >> 16);
+          a[mt][2 * q][0] = e4m3x2_to_f16x2(v0.x);
+          a[mt][2 * q][1] = e4m3x2_to_f16x2(v1.x);
+          a[mt][2 * q][2] = e4m3x2_to_f16x2(v0.x >> 16);
+          a[mt][2 * q][3] = e4m3x2_to_f16x2(v1.x >> 16);
+          a[mt][2 * q + 1][0] = e4m3x2_to_f16x2(v0.y);
+          a[mt][2 * q + 1][1] = e4m3x2_to_f16x2(v1.y);
+          a[mt][2 * q + 1][2] = e4m3x2_to_f16x2(v0.y >> 16);
+          a[mt][2 * q + 1][3] = e4m3x2_to_f16x2(v1.y >> 16);
         }
       }
-      {
-        const int off = F::kRopeOff + 16 * w + 4 * c;
-        const uint32_t x0 = *reinterpret_cast<const uint32_t*>(row0 + off);
-        const uint32_t x1 = *reinterpret_cast<const uint32_t*>(row1 + off);
-        a[8][0] = e4m3x2_to_f16x2(x0);
-        a[8][1] = e4m3x2_to_f16x2(x1);
-        a[8][2] = e4m3x2_to_f16x2(x0 >> 16);
-        a[8][3] = e4m3x2_to_f16x2(x1 >> 16);
-      }
+      const int roff = F::kRopeOff + 16 * w + 4 * c;
+      const uint32_t x0 = *reinterpret_cast<const uint32_t*>(row0 + roff);
+      const uint32_t x1 = *reinterpret_cast<const uint32_t*>(row1 + roff);
+      a[mt][8][0] = e4m3x2_to_f16x2(x0);
+      a[mt][8][1] = e4m3x2_to_f16x2(x1);
+      a[mt][8][2] = e4m3x2_to_f16x2(x0 >> 16);
+      a[mt][8][3] = e4m3x2_to_f16x2(x1 >> 16);
+    }
 
-      // Partial scores over this warp's 144 dims: S^T [16 tokens x 16 heads].
-      float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      float sodd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // second chain: shorter dependency
+    // ---- partial scores over this warp's 144 dims: S^T [32 tokens x 16 heads]
+    float sacc[2][2][4];
 #pragma unroll
-      for (int ks = 0; ks < 9; ks += 2) {
-        mma_f16(sacc[0], a[ks], bq[ks][0][0], bq[ks][0][1]);
-        mma_f16(sacc[1], a[ks], bq[ks][1][0], bq[ks][1][1]);
-        if (ks + 1 < 9) {
-          mma_f16(sodd[0], a[ks + 1], bq[ks + 1][0][0], bq[ks + 1][0][1]);
-          mma_f16(sodd[1], a[ks + 1], bq[ks + 1][1][0], bq[ks + 1][1][1]);
-        }
-      }
+    for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-      for (int n = 0; n < 2; ++n)
+      for (int n = 0; n < 2; ++n) sacc[mt][n][0] = sacc[mt][n][1] = sacc[mt][n][2] = sacc[mt][n][3] = 0.f;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[n][e] += sodd[n][e];
+    for (int ks = 0; ks < kKSteps; ++ks) {
+      const uint4 qb = sm.qfrag[w][ks][lane];
 #pragma unroll
-      for (int n = 0; n < 2; ++n) {
-        *reinterpret_cast<float2*>(&sm.red[w][g][8 * n + 2 * c]) = make_float2(sacc[n][0], sacc[n][1]);
-        *reinterpret_cast<float2*>(&sm.red[w][g + 8][8 * n + 2 * c]) = make_float2(sacc[n][2], sacc[n][3]);
-      }
-      named_bar_sync(1, kConsumerWarps * 32);
-      if (sm.abort_flag) {
-        aborted = true;
-        break;
-      }
-
-      // Head owner: heads hown, hown+1 for token tloc of this m-tile.
-      {
-        float2 s = *reinterpret_cast<const float2*>(&sm.red[0][tloc][hown]);
-#pragma unroll
-        for (int ww = 1; ww < kConsumerWarps; ++ww) {
-          const float2 v = *reinterpret_cast<const float2*>(&sm.red[ww][tloc][hown]);
-          s.x += v.x;
-          s.y += v.y;
-        }
-        const bool valid = sm.tok_all[it * kStageRows + 16 * mt + tloc] >= 0;
-        float z[2] = {valid ? s.x * args.scale_log2 : -INFINITY, valid ? s.y * args.scale_log2 : -INFINITY};
-        __half ph[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float mx = z[e];
-#pragma unroll
-          for (int off = 2; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-          const float m_new = fmaxf(m_run[e], mx);
-          const float alpha = (m_new == -INFINITY) ? 1.f : ex2(m_run[e] - m_new);
-          const float p = (z[e] == -INFINITY) ? 0.f : ex2(z[e] - m_new);
-          ph[e] = __float2half_rn(p);
-          l_run[e] = l_run[e] * alpha + __half2float(ph[e]);
-          m_run[e] = m_new;
-          if (tloc == 0) sm.alpha[hown + e] = alpha;
-        }
-        sm.pbuf[hown][tloc] = ph[0];
-        sm.pbuf[hown + 1][tloc] = ph[1];
-      }
-      named_bar_sync(1, kConsumerWarps * 32);
-
-      // O[16 heads x 128 dims] += P[16 x 16 tokens] . V[16 tokens x 128 dims].
-      uint32_t pa[4];
-      ldmatrix_x4(pa, smem_u32(&sm.pbuf[lane & 15][(lane >> 4) * 8]));
-      const float al0 = sm.alpha[g];
-      const float al1 = sm.alpha[g + 8];
-      if (__any_sync(0xFFFFFFFFu, al0 != 1.f || al1 != 1.f)) {
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-#pragma unroll
-          for (int be = 0; be < 2; ++be) {
-            o[ks][be][0] *= al0;
-            o[ks][be][1] *= al0;
-            o[ks][be][2] *= al1;
-            o[ks][be][3] *= al1;
-          }
-      }
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        mma_f16(o[ks][0], pa, movmatrix_t(a[ks][0]), movmatrix_t(a[ks][1]));
-        mma_f16(o[ks][1], pa, movmatrix_t(a[ks][2]), movmatrix_t(a[ks][3]));
+      for (int mt = 0; mt < 2; ++mt) {
+        mma_f16(sacc[mt][0], a[mt][ks], qb.x, qb.y);
+        mma_f16(sacc[mt][1], a[mt][ks], qb.z, qb.w);
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.empty[slot]);
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int n = 0; n < 2; ++n) {
+        *reinterpret_cast<float2*>(&sm.red[w][16 * mt + g][8 * n + 2 * c]) = make_float2(sacc[mt][n][0], sacc[mt][n][1]);
+        *reinterpret_cast<float2*>(&sm.red[w][16 * mt + g + 8][8 * n + 2 * c]) =
+            make_float2(sacc[mt][n][2], sacc[mt][n][3]);
+      }
+    named_bar_sync(1, kConsumerWarps * 32);
+    if (sm.abort_flag) {
+      aborted = true;
+      abort_it = it;
+      break;
+    }
+    // Every warp has finished reading the rows of stages <= it, so stages up
+    // to it + kStages may be issued; at most two per boundary.
+    for (int k = 0; k < 2 && next_fill < n_stages && next_fill <= it + kStages; ++k) fill_stage(next_fill++);
+
+    // ---- head owner: heads 4w..4w+3 of token `lane`
+    {
+      float4 s4 = *reinterpret_cast<const float4*>(&sm.red[0][lane][4 * w]);
+#pragma unroll
+      for (int ww = 1; ww < kConsumerWarps; ++ww) {
+        const float4 v = *reinterpret_cast<const float4*>(&sm.red[ww][lane][4 * w]);
+        s4.x += v.x;
+        s4.y += v.y;
+        s4.z += v.z;
+        s4.w += v.w;
+      }
+      const bool valid = sm.tok_all[it * kStageRows + lane] >= 0;
+      float z[4] = {s4.x, s4.y, s4.z, s4.w};
+      bool need = false;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        z[e] = valid ? z[e] * args.scale_log2 : -INFINITY;
+        need |= z[e] > m_ref[e] + kLazy;
+      }
+      float alpha[4] = {1.f, 1.f, 1.f, 1.f};
+      if (__any_sync(0xFFFFFFFFu, need)) {  // rare: raise the reference maxima
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float mx = z[e];
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+          if (mx > m_ref[e] + kLazy) {
+            alpha[e] = ex2(m_ref[e] - mx);  // 0 when m_ref was -inf (nothing accumulated yet)
+            m_ref[e] = mx;
+          }
+        }
+      }
+      int any_rescale = 0;
+      __half ph[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float p = (z[e] == -INFINITY) ? 0.f : ex2(z[e] - m_ref[e]);
+        ph[e] = __float2half_rn(p);
+        l_run[e] = l_run[e] * alpha[e] + __half2float(ph[e]);
+        sm.pbuf[4 * w + e][lane] = ph[e];
+        any_rescale |= alpha[e] != 1.f;
+      }
+      if (lane == 0) {
+        *reinterpret_cast<float4*>(&sm.alpha[4 * w]) = make_float4(alpha[0], alpha[1], alpha[2], alpha[3]);
+        sm.rescale[w] = any_rescale;
+      }
+    }
+    named_bar_sync(1, kConsumerWarps * 32);
+
+    // ---- O[16 heads x 128 dims] += P[16 x 32 tokens] . V[32 tokens x 128 dims]
+    const int4 rf = *reinterpret_cast<const int4*>(sm.rescale);
+    if (rf.x | rf.y | rf.z | rf.w) {
+      const float al0 = sm.alpha[g];
+      const float al1 = sm.alpha[g + 8];
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+        for (int be = 0; be < 2; ++be) {
+          o[ks][be][0] *= al0;
+          o[ks][be][1] *= al0;
+          o[ks][be][2] *= al1;
+          o[ks][be][3] *= al1;
+        }
+    }
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      uint32_t pa[4];
+      ldmatrix_x4(pa, smem_u32(&sm.pbuf[lane & 15][16 * mt + (lane >> 4) * 8]));
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        mma_f16(o[ks][0], pa, movmatrix_t(a[mt][ks][0]), movmatrix_t(a[mt][ks][1]));
+        mma_f16(o[ks][1], pa, movmatrix_t(a[mt][ks][2]), movmatrix_t(a[mt][ks][3]));
+      }
+    }
   }
-  if (aborted) return;
+  if (aborted) {
+    // Leave no copy in flight: wait (bounded) for the stages issued but not
+    // yet consumed (abort_it .. next_fill - 1).
+    for (int it2 = abort_it; it2 < next_fill; ++it2)
+        mbar_wait_bounded(&sm.full[it2 % kStages], static_cast<uint32_t>(it2 / kStages) & 1u, args.fault_word,
+                          kFaultDecodeWait);
+    return;
+  }
 
   // ---------------------------------------------------------------- finish
 #pragma unroll
-  for (int e = 0; e < 2; ++e) {
+  for (int e = 0; e < 4; ++e) {
     float l = l_run[e];
 #pragma unroll
-    for (int off = 2; off < 32; off <<= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, off);
-    if (tloc == 0) {
-      sm.mfin[hown + e] = m_run[e];
-      sm.lfin[hown + e] = l;
+    for (int off = 1; off < 32; off <<= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, off);
+    if (lane == 0) {
+      sm.mfin[4 * w + e] = m_ref[e];
+      sm.lfin[4 * w + e] = l;
     }
   }
   named_bar_sync(1, kConsumerWarps * 32);
 
-  const int h0 = hg * kHeadsPerCta + g;  // rows g and g+8 of this thread's O fragments
+  // rows g and g+8 of this thread's O fragments are heads h0 and h0 + 8
   const float l0 = sm.lfin[g], l1 = sm.lfin[g + 8];
   const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f;
   const float inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
@@ -474,6 +498,9 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_decode_kernel(const Decode
 __global__ void __launch_bounds__(128) splitk_merge_kernel(const float* __restrict__ part_o,
                                                            const float* __restrict__ part_lse, int splits,
                                                            uint16_t* __restrict__ out, float* __restrict__ lse) {
+  // Launched as a programmatic dependent of the decode: wait until that grid
+  // has completed and its partials are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t bh = blockIdx.x;
   const int t = threadIdx.x;
   const float* pl = part_lse + bh * splits;
@@ -579,7 +606,19 @@ cudaError_t launch_sparse_decode(int fmt, const uint16_t* q_nope, const uint16_t
   cudaError_t e = fmt == 0 ? launch_fmt<0>(a, batch, stream) : launch_fmt<1>(a, batch, stream);
   if (e != cudaSuccess || plan.splits == 1) return e;
   const int64_t n_bh = static_cast<int64_t>(batch) * num_heads;
-  splitk_merge_kernel<<<static_cast<unsigned>(n_bh), 128, 0, stream>>>(a.part_o, a.part_lse, plan.splits, out, lse);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(n_bh));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, splitk_merge_kernel, static_cast<const float*>(a.part_o),
+                         static_cast<const float*>(a.part_lse), plan.splits, out, lse);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
