@@ -51,6 +51,9 @@ def parse():
     p.add_argument("--no-extras", action="store_true", help="skip the append / indexer sub-measurements")
     p.add_argument("--ctx", type=int, default=140_000,
                    help="context length per request (smaller values only shrink the pools, for profiling)")
+    p.add_argument("--append-sessions", type=int, default=64, help="sessions in the quantize-on-write sub-benchmark")
+    p.add_argument("--indexer-batch", type=int, default=64, help="requests in the indexer + top-k sub-benchmark")
+    p.add_argument("--only-extras", action="store_true", help="time only the sub-benchmarks (profiling)")
     return p.parse_args()
 
 
@@ -244,6 +247,10 @@ def main():
         pg = dist
 
     hbm, tf_burst, tf_sust, peak_kind = peaks()
+    if args.only_extras:
+        stream = torch.cuda.Stream(device=dev)
+        print(json.dumps(sub_measurements(m, W, dev, stream, args, hbm)), flush=True)
+        return
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     B, H, K = 32, 16, 2048
     layer_bytes4 = decode_bytes(B, H, K, ROW_NVFP4)
@@ -412,7 +419,7 @@ def sub_measurements(m, W, dev, stream, args, hbm):
     """Quantize-on-write and indexer + top-k, each timed with CUDA events."""
     import torch
     out = {}
-    wl = W.append_turn(dev)
+    wl = W.append_turn(dev, sessions=args.append_sessions)
     n = wl.slot_mapping.numel()
     res = {}
     for fmt, rb in ((0, ROW_NVFP4), (1, ROW_FP8)):
@@ -438,10 +445,11 @@ def sub_measurements(m, W, dev, stream, args, hbm):
     del wl
     torch.cuda.empty_cache()
 
-    iw = W.indexer_keys(dev, seed=0, batch=64, ctx=140_000, n_heads=32, topk=2048)
+    nb = args.indexer_batch
+    iw = W.indexer_keys(dev, seed=0, batch=nb, ctx=140_000, n_heads=32, topk=2048)
     max_ctx = 140_000
-    ws = torch.empty(m.mla_indexer_topk_workspace_size(64, max_ctx, 2048), dtype=torch.uint8, device=dev)
-    tk = torch.empty((64, 2048), dtype=torch.int32, device=dev)
+    ws = torch.empty(m.mla_indexer_topk_workspace_size(nb, max_ctx, 2048), dtype=torch.uint8, device=dev)
+    tk = torch.empty((nb, 2048), dtype=torch.int32, device=dev)
 
     def run():
         m.mla_indexer_topk(iw.q_idx, iw.head_w, iw.key_pool, iw.key_stride, iw.num_blocks, iw.block_table,
@@ -457,7 +465,7 @@ def sub_measurements(m, W, dev, stream, args, hbm):
         e1.record(stream)
     e1.synchronize()
     t = e0.elapsed_time(e1) / args.steps * 1e-3
-    tokens = 64 * 140_000
+    tokens = nb * 140_000
     key_bytes = tokens * 132
     out["indexer_topk"] = {"workload": iw.name, "us": t * 1e6, "tokens_per_s": tokens / t,
                            "key_hbm_gbs": key_bytes / t / 1e9, "frac": key_bytes / t / 1e9 / hbm}

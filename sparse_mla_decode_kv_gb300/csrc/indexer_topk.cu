@@ -14,11 +14,14 @@
 // shuffles.  HBM-bound at 132 bytes per token.
 //
 // topk_kernel: one 1,024-thread CTA per request.  Scores map to order-
-// preserving 32-bit keys (with -0.0 folded into +0.0); three histogram
-// passes over 11 + 11 + 10 key bits find the k-th largest key T and how
-// many ties at T are taken; a final pass writes every index with key > T and
-// the lowest-index ties, in ascending index order, using block-wide prefix
-// counts.  The scores stay L2-resident between passes.
+// preserving 32-bit keys (with -0.0 folded into +0.0).  A sorted strided
+// sample of 2,048 keys picks a threshold expected to keep ~2.5 k elements; one
+// pass over the row collects the elements at or above it into per-warp lists
+// in index order; three histogram passes over 11 + 11 + 10 key bits then find
+// the k-th largest key T among the candidates and how many ties at T are
+// taken, and an ordered compaction writes every index with key > T and the
+// lowest-index ties in ascending order.  If the threshold keeps too few or
+// too many elements, the same selection runs over the whole row instead.
 #include <cuda_fp16.h>
 
 #include "mla_device.cuh"
@@ -64,7 +67,7 @@ __device__ __forceinline__ const uint8_t* key_row(const IdxArgs& a, const int32_
 }
 
 template <int NT>  // n-tiles of 8 heads
-__global__ void __launch_bounds__(kIdxWarps * 32) indexer_scores_kernel(const IdxArgs a) {
+__global__ void __launch_bounds__(kIdxWarps * 32, 3) indexer_scores_kernel(const IdxArgs a) {
   const int b = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
@@ -95,19 +98,33 @@ __global__ void __launch_bounds__(kIdxWarps * 32) indexer_scores_kernel(const Id
 
   float* out_row = a.scores + static_cast<int64_t>(b) * a.scores_stride;
   const int n_mt = kIdxTokensPerCta / 16;
-  for (int mt = warp; mt < n_mt; mt += kIdxWarps) {
+  // Software pipeline: the keys and scales of the warp's next m-tile are
+  // loaded while the current one is multiplied.
+  auto load_tile = [&](int mt, uint2 (&v0)[4], uint2 (&v1)[4], float& s0, float& s1, bool& ok0, bool& ok1) {
     const int t0 = t_begin + 16 * mt + g;
-    const int t1 = t0 + 8;
-    if (t_begin + 16 * mt >= ctx) break;
-    float s0 = 0.f, s1 = 0.f;
     const uint8_t* k0 = key_row(a, bt_row, t0, ctx, &s0);
-    const uint8_t* k1 = key_row(a, bt_row, t1, ctx, &s1);
-    uint2 v0[4], v1[4];
+    const uint8_t* k1 = key_row(a, bt_row, t0 + 8, ctx, &s1);
+    ok0 = k0 != nullptr;
+    ok1 = k1 != nullptr;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       v0[q] = k0 ? __ldg(reinterpret_cast<const uint2*>(k0 + 32 * q + 8 * c)) : make_uint2(0, 0);
       v1[q] = k1 ? __ldg(reinterpret_cast<const uint2*>(k1 + 32 * q + 8 * c)) : make_uint2(0, 0);
     }
+  };
+  uint2 v0[4], v1[4];
+  float s0 = 0.f, s1 = 0.f;
+  bool ok0 = false, ok1 = false;
+  int mt = warp;
+  if (t_begin + 16 * mt < ctx) load_tile(mt, v0, v1, s0, s1, ok0, ok1);
+  for (; mt < n_mt && t_begin + 16 * mt < ctx; mt += kIdxWarps) {
+    const int t0 = t_begin + 16 * mt + g;
+    const int t1 = t0 + 8;
+    const int nmt = mt + kIdxWarps;
+    uint2 n0[4], n1[4];
+    float ns0 = 0.f, ns1 = 0.f;
+    bool nok0 = false, nok1 = false;
+    if (nmt < n_mt && t_begin + 16 * nmt < ctx) load_tile(nmt, n0, n1, ns0, ns1, nok0, nok1);
     float acc[NT][4];
 #pragma unroll
     for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
@@ -135,9 +152,18 @@ __global__ void __launch_bounds__(kIdxWarps * 32) indexer_scores_kernel(const Id
     p1 += __shfl_xor_sync(0xFFFFFFFFu, p1, 1);
     p1 += __shfl_xor_sync(0xFFFFFFFFu, p1, 2);
     if (c == 0) {
-      if (t0 < ctx) out_row[t0] = k0 ? p0 : -INFINITY;
-      if (t1 < ctx) out_row[t1] = k1 ? p1 : -INFINITY;
+      if (t0 < ctx) out_row[t0] = ok0 ? p0 : -INFINITY;
+      if (t1 < ctx) out_row[t1] = ok1 ? p1 : -INFINITY;
     }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      v0[q] = n0[q];
+      v1[q] = n1[q];
+    }
+    s0 = ns0;
+    s1 = ns1;
+    ok0 = nok0;
+    ok1 = nok1;
   }
 }
 
@@ -206,88 +232,220 @@ __device__ __forceinline__ uint32_t select_bin(const uint32_t* hist, uint32_t ne
   return *sel_bin;
 }
 
+// Sample-select parameters: a strided sample of kSample keys fixes a
+// threshold T0 expected to keep ~2.5 k elements; one order-preserving pass
+// collects every element >= T0 into per-warp lists (warp w scans a contiguous
+// chunk, so concatenating the lists keeps index order); the exact selection
+// then runs on the candidates in shared memory.  If a list overflows or fewer
+// than k elements reach T0, the kernel falls back to radix passes over the
+// whole row.
+constexpr int kSample = 2048;
+constexpr int kTopkWarps = kTopkThreads / 32;
+constexpr int kWarpCap = 512;
+constexpr int kCandCap = kWarpCap * kTopkWarps;  // 16,384 candidates
+
+struct TopkSmem {
+  uint32_t cand_key[kCandCap];
+  int32_t cand_idx[kCandCap];
+  uint32_t sample[kSample];
+  uint32_t hist[kHistBins];
+  uint32_t warp_sums[32];
+  uint32_t warp_cnt[32];
+  uint32_t warp_off[32];
+  uint32_t sel_bin, sel_need, run_gt, run_eq;
+};
+
+// Exact selection over `count` elements given in ascending index order by
+// `src(j) -> (order key, index)`: three radix passes find the k-th largest key
+// T and how many ties at T are taken, then an ordered compaction writes every
+// element with key > T and the lowest-index ties, ascending, to orow[0..k).
+template <class Src>
+__device__ void select_and_compact(const Src& src, int count, int topk, int32_t* orow, TopkSmem& sm) {
+  const int tid = threadIdx.x;
+  uint32_t prefix = 0, need = topk;
+  const int shifts[3] = {21, 10, 0};
+  const uint32_t widths[3] = {11, 11, 10};
+  for (int pass = 0; pass < 3; ++pass) {
+    for (int j = tid; j < kHistBins; j += kTopkThreads) sm.hist[j] = 0;
+    __syncthreads();
+    const int sh = shifts[pass];
+    const uint32_t bmask = (1u << widths[pass]) - 1u;
+    const int hi_shift = sh + static_cast<int>(widths[pass]);
+    for (int base = 0; base < count; base += 4 * kTopkThreads) {
+      uint32_t key[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = base + u * kTopkThreads + tid;
+        key[u] = j < count ? src.key(j) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = base + u * kTopkThreads + tid;
+        const bool match = j < count && (pass == 0 || (key[u] >> hi_shift) == prefix);
+        hist_add(sm.hist, (key[u] >> sh) & bmask, match);
+      }
+    }
+    __syncthreads();
+    if (tid == 0) sm.sel_bin = sm.sel_need = 0;
+    __syncthreads();
+    const uint32_t bin = select_bin(sm.hist, need, sm.warp_sums, &sm.sel_bin, &sm.sel_need);
+    need = sm.sel_need;
+    prefix = (pass == 0) ? bin : ((prefix << widths[pass]) | bin);
+    __syncthreads();
+  }
+  const uint32_t T = prefix;
+  // element j goes to position G(j) + min(E(j), need), G / E counting keys > T / == T before j
+  if (tid == 0) sm.run_gt = sm.run_eq = 0;
+  __syncthreads();
+  constexpr int kPer = 4;
+  for (int base = 0; base < count; base += kTopkThreads * kPer) {
+    uint32_t keys[kPer];
+    uint32_t ngt = 0, neq = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int j = base + tid * kPer + i;
+      keys[i] = j < count ? src.key(j) : 0u;
+      ngt += (j < count && keys[i] > T);
+      neq += (j < count && keys[i] == T);
+    }
+    uint32_t tot;
+    const uint32_t packed = block_exclusive_scan((ngt << 16) | neq, sm.warp_sums, &tot);
+    uint32_t G = sm.run_gt + (packed >> 16), E = sm.run_eq + (packed & 0xFFFFu);
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int j = base + tid * kPer + i;
+      if (j >= count) break;
+      if (keys[i] > T) {
+        orow[G + min(E, need)] = src.idx(j);
+        ++G;
+      } else if (keys[i] == T) {
+        if (E < need) orow[G + E] = src.idx(j);
+        ++E;
+      }
+    }
+    __syncthreads();
+    if (tid == 0) {
+      sm.run_gt += tot >> 16;
+      sm.run_eq += tot & 0xFFFFu;
+    }
+    __syncthreads();
+  }
+}
+
+struct RowSrc {
+  const float* row;
+  __device__ uint32_t key(int j) const { return order_key(__ldg(row + j)); }
+  __device__ int32_t idx(int j) const { return j; }
+};
+struct CandSrc {
+  const TopkSmem* sm;
+  __device__ uint32_t key(int j) const { return sm->cand_key[j]; }
+  __device__ int32_t idx(int j) const { return sm->cand_idx[j]; }
+};
+
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restrict__ scores, int64_t row_stride,
                                                             const int32_t* __restrict__ ctx_lens, int topk,
                                                             int max_ctx, int32_t* __restrict__ out) {
-  __shared__ uint32_t hist[kHistBins];
-  __shared__ uint32_t warp_sums[32];
-  __shared__ uint32_t sel_bin, sel_need;
-  __shared__ uint32_t run_gt, run_eq;
+  extern __shared__ __align__(16) uint8_t topk_smem_raw[];
+  TopkSmem& sm = *reinterpret_cast<TopkSmem*>(topk_smem_raw);
   const int b = blockIdx.x;
   const int n = max(0, min(__ldg(ctx_lens + b), max_ctx));
   const float* row = scores + static_cast<int64_t>(b) * row_stride;
   int32_t* orow = out + static_cast<int64_t>(b) * topk;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   if (n <= topk) {  // everything is selected
     for (int j = tid; j < topk; j += kTopkThreads) orow[j] = j < n ? j : -1;
     return;
   }
 
-  // Three radix passes: key bits [31:21], [20:10], [9:0].
-  uint32_t prefix = 0, need = topk;
-  const int shifts[3] = {21, 10, 0};
-  const uint32_t widths[3] = {11, 11, 10};
-  for (int pass = 0; pass < 3; ++pass) {
-    for (int j = tid; j < kHistBins; j += kTopkThreads) hist[j] = 0;
-    __syncthreads();
-    const int sh = shifts[pass];
-    const uint32_t bmask = (1u << widths[pass]) - 1u;
-    const int hi_shift = sh + static_cast<int>(widths[pass]);  // bits above this pass must equal `prefix`
-    for (int base = 0; base < n; base += kTopkThreads) {
-      const int j = base + tid;
-      const bool in = j < n;
-      const uint32_t key = in ? order_key(__ldg(row + j)) : 0u;
-      const bool match = in && (pass == 0 || (key >> hi_shift) == prefix);
-      hist_add(hist, (key >> sh) & bmask, match);
-    }
-    __syncthreads();
-    if (tid == 0) sel_bin = sel_need = 0;
-    __syncthreads();
-    const uint32_t bin = select_bin(hist, need, warp_sums, &sel_bin, &sel_need);
-    need = sel_need;
-    prefix = (pass == 0) ? bin : ((prefix << widths[pass]) | bin);
-    __syncthreads();
-  }
-  const uint32_t T = prefix;  // the k-th largest key; `need` ties at T are taken
-
-  // Compaction in index order: element j goes to position G(j) + min(E(j), need)
-  // where G / E count the keys > T / == T before j.
-  if (tid == 0) run_gt = run_eq = 0;
+  // 1. Strided sample, sorted descending (bitonic, one pair per thread).
+  for (int i = tid; i < kSample; i += kTopkThreads)
+    sm.sample[i] = order_key(__ldg(row + static_cast<int>((static_cast<int64_t>(i) * n) / kSample)));
   __syncthreads();
-  constexpr int kPer = 4;
-  for (int base = 0; base < n; base += kTopkThreads * kPer) {
-    uint32_t keys[kPer];
-    uint32_t ngt = 0, neq = 0;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int j = base + tid * kPer + i;
-      keys[i] = j < n ? order_key(__ldg(row + j)) : 0u;
-      ngt += (j < n && keys[i] > T);
-      neq += (j < n && keys[i] == T);
-    }
-    uint32_t tot;
-    const uint32_t packed = block_exclusive_scan((ngt << 16) | neq, warp_sums, &tot);
-    uint32_t G = run_gt + (packed >> 16), E = run_eq + (packed & 0xFFFFu);
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int j = base + tid * kPer + i;
-      if (j >= n) break;
-      if (keys[i] > T) {
-        orow[G + min(E, need)] = j;
-        ++G;
-      } else if (keys[i] == T) {
-        if (E < need) orow[G + E] = j;
-        ++E;
+  for (int size = 2; size <= kSample; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const int i = 2 * tid - (tid & (stride - 1));  // lower index of this thread's pair
+      const int j = i + stride;
+      const bool desc = (i & size) == 0;             // direction of this sub-sequence
+      const uint32_t a = sm.sample[i], c = sm.sample[j];
+      if ((a < c) == desc) {
+        sm.sample[i] = c;
+        sm.sample[j] = a;
       }
+      __syncthreads();
     }
-    __syncthreads();
-    if (tid == 0) {
-      run_gt += tot >> 16;
-      run_eq += tot & 0xFFFFu;
-    }
-    __syncthreads();
   }
+  const int r0 = min(kSample - 1, static_cast<int>((2.5 * topk * kSample) / n) + 8);
+  const uint32_t T0 = sm.sample[r0];
+
+  // 2. Collect elements >= T0, order-preserving per warp chunk.
+  const int chunk = (n + kTopkWarps - 1) / kTopkWarps;
+  const int lo = warp * chunk, hi = min(n, lo + chunk);
+  uint32_t cnt = 0;
+  constexpr int kBatch = 8;  // independent loads in flight per lane
+  for (int base = lo; base < hi; base += 32 * kBatch) {
+    uint32_t key[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int j = base + 32 * u + lane;
+      key[u] = j < hi ? order_key(__ldg(row + j)) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int j = base + 32 * u + lane;
+      const bool take = j < hi && key[u] >= T0;
+      const uint32_t m = __ballot_sync(0xFFFFFFFFu, take);
+      const uint32_t pos = cnt + __popc(m & ((1u << lane) - 1u));
+      if (take && pos < kWarpCap) {
+        sm.cand_key[warp * kWarpCap + pos] = key[u];
+        sm.cand_idx[warp * kWarpCap + pos] = j;
+      }
+      cnt += __popc(m);
+    }
+  }
+  if (lane == 0) sm.warp_cnt[warp] = cnt;
+  __syncthreads();
+  uint32_t total = 0, overflow = 0, my_off = 0;
+#pragma unroll 1
+  for (int w = 0; w < kTopkWarps; ++w) {
+    const uint32_t cw = sm.warp_cnt[w];
+    if (w == warp) my_off = total;
+    total += cw;
+    overflow |= cw > static_cast<uint32_t>(kWarpCap);
+  }
+  if (overflow || total < static_cast<uint32_t>(topk)) {
+    // Rare: fall back to exact selection over the whole row.
+    select_and_compact(RowSrc{row}, n, topk, orow, sm);
+    return;
+  }
+  if (lane == 0) sm.warp_off[warp] = my_off;
+  __syncthreads();
+
+  // 3. Concatenate the lists in warp order (elements only move down).
+  constexpr int kPerThread = kCandCap / kTopkThreads;
+  uint32_t kk[kPerThread];
+  int32_t ii[kPerThread];
+  int dst[kPerThread];
+#pragma unroll
+  for (int e = 0; e < kPerThread; ++e) {
+    const int srcpos = tid + e * kTopkThreads;
+    const int w = srcpos / kWarpCap, o = srcpos % kWarpCap;
+    dst[e] = (o < static_cast<int>(sm.warp_cnt[w])) ? static_cast<int>(sm.warp_off[w]) + o : -1;
+    kk[e] = sm.cand_key[srcpos];
+    ii[e] = sm.cand_idx[srcpos];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int e = 0; e < kPerThread; ++e)
+    if (dst[e] >= 0) {
+      sm.cand_key[dst[e]] = kk[e];
+      sm.cand_idx[dst[e]] = ii[e];
+    }
+  __syncthreads();
+
+  // 4. Exact selection among the candidates (all in shared memory).
+  select_and_compact(CandSrc{&sm}, static_cast<int>(total), topk, orow, sm);
 }
 
 }  // namespace
@@ -297,7 +455,18 @@ size_t topk_workspace_bytes(int, int, int) { return 0; }
 cudaError_t launch_topk(const float* scores, int64_t row_stride, const int32_t* context_lens, int batch, int topk,
                         int max_context_len, int32_t* out, void*, cudaStream_t stream) {
   if (batch <= 0) return cudaSuccess;
-  topk_kernel<<<batch, kTopkThreads, 0, stream>>>(scores, row_stride, context_lens, topk, max_context_len, out);
+  static int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(TopkSmem)));
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  topk_kernel<<<batch, kTopkThreads, sizeof(TopkSmem), stream>>>(scores, row_stride, context_lens, topk,
+                                                                  max_context_len, out);
   return cudaGetLastError();
 }
 
