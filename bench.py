@@ -67,6 +67,34 @@ def peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
+# DRAM traffic of one NVFP4 decode launch of the TP4-rank workload
+# (dram__bytes_read.sum + dram__bytes_write.sum from one ncu capture of 65,536
+# selected rows; profiles/sparse_decode_nvfp4_tp4_rank.md), and a digest of
+# the kernel source it was taken on: once the source differs, the figure no
+# longer describes the kernel and is reported as null.
+DECODE_NVFP4_TRAFFIC = {"bytes": 29_474_560 + 6_144, "source_digest": "d36012b0acf10993"}
+KERNEL_SOURCES = ("sparse_mla_decode_kv_gb300/csrc/sparse_decode.cu", "sparse_mla_decode_kv_gb300/csrc/mla_device.cuh")
+
+
+def kernel_source_digest():
+    """sha256 over the decode kernel's sources with comments and blank lines
+    removed (a comment edit does not change the kernel)."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        for line in open(os.path.join(ROOT, rel)):
+            code = re.sub(r"//.*$", "", line).strip()
+            if code:
+                h.update(code.encode() + b"\n")
+    return h.hexdigest()[:16]
+
+
+def decode_traffic():
+    t = DECODE_NVFP4_TRAFFIC
+    return t["bytes"] if kernel_source_digest() == t["source_digest"] else None
+
+
 def decode_bytes(batch, heads, topk, row_bytes):
     """Algorithmic bytes of one decode layer: every selected row plus its int32
     index, and per (request, head) the bf16 query (576 values), bf16 output
@@ -77,6 +105,23 @@ def decode_bytes(batch, heads, topk, row_bytes):
 def decode_flops(batch, heads, topk):
     """2 * (576 + 512) FLOP per head per selected row (QK over 576, PV over 512)."""
     return batch * heads * topk * 2 * (576 + 512)
+
+
+def max_over_ranks(x, dist=None, device=None):
+    """The slowest rank's value of a per-rank time (a no-op on one rank).
+    Every rank gets the maximum back."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t)
+
+
+def whole_job_rate(units_per_rank, world, seconds):
+    """Units processed by all ranks (each runs its own replica) per second of
+    the slowest rank's time."""
+    return units_per_rank * world / seconds
 
 
 class ClockSampler:
@@ -309,12 +354,7 @@ def main():
             e1.record(stream)
         e1.synchronize()
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / steps
-        if pg:
-            t = torch.tensor([ms], device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            ms = float(t)
-        return ms
+        return max_over_ranks(e0.elapsed_time(e1) / steps, pg, dev)
 
     props = torch.cuda.get_device_properties(dev)
     pci = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
@@ -328,7 +368,7 @@ def main():
     per_layer4 = ms4 / L * 1e-3
     per_layer8 = ms8 / L * 1e-3
     rows = B * K
-    value = rows * world / per_layer4
+    value = whole_job_rate(rows, world, per_layer4)
     ach4 = layer_bytes4 / per_layer4 / 1e9
     ach8 = layer_bytes8 / per_layer8 / 1e9
     fl = decode_flops(B, H, K)
@@ -368,12 +408,8 @@ def main():
             e2e_step()
         e1.record(stream)
     e1.synchronize()
-    ms_e2e = e0.elapsed_time(e1) / args.steps
-    if pg:
-        t = torch.tensor([ms_e2e], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_e2e = float(t)
-    e2e_value = rows * L * world / (ms_e2e * 1e-3)
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, pg, dev)
+    e2e_value = whole_job_rate(rows * L, world, ms_e2e * 1e-3)
 
     extras = {}
     if not args.no_extras:
@@ -393,12 +429,12 @@ def main():
         "per_layer_us": per_layer4 * 1e6,
         "hbm_gbs": ach4,
         "roofline": {"bound": "hbm" if layer_bytes4 / hbm / 1e9 >= fl / tf_burst / 1e12 else "tensor",
-                     "achieved": ach4, "peak": hbm, "unit": "GB/s", "frac": ach4 / hbm, "traffic": None,
+                     "achieved": ach4, "peak": hbm, "unit": "GB/s", "frac": ach4 / hbm, "traffic": decode_traffic(),
                      "kernel": "sparse_decode_kernel<NVFP4> + splitk_merge_kernel (one decode layer)",
                      "algorithmic_bytes_per_launch": layer_bytes4, "peak_source": peak_kind,
                      "roofline_us": roof_t4 * 1e6, "frac_of_roofline_time": roof_t4 / per_layer4,
                      "vs_nominal_8tbs": ach4 / 8000.0},
-        "fp8": {"value": rows * world / per_layer8, "unit": UNIT, "per_layer_us": per_layer8 * 1e6,
+        "fp8": {"value": whole_job_rate(rows, world, per_layer8), "unit": UNIT, "per_layer_us": per_layer8 * 1e6,
                 "hbm_gbs": ach8, "frac": ach8 / hbm, "roofline_us": roof_t8 * 1e6,
                 "bytes_per_row": ROW_FP8 + 4},
         "nvfp4_bytes_per_row": ROW_NVFP4 + 4,

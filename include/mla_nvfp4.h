@@ -228,7 +228,8 @@ mla_status_t mla_topk(const float* scores, int64_t score_row_stride, const int32
  *                 b * idx_block_stride holds block_size x 128 key bytes
  *                 followed by block_size float scales
  *   idx_block_stride  bytes, a multiple of 16, >= block_size * 132
- *   n_idx_heads   8, 16, 24, ..., 64
+ *   n_idx_heads   8, 16, 32 or 64 (other multiples of 8 up to 64 return
+ *                 MLA_ERR_UNSUPPORTED, anything else MLA_ERR_INVALID_ARG)
  *   topk_out      device int32 [batch, topk]
  *   scores_out    device float [batch, max_context_len] (entries past a
  *                 request's context are left untouched), or NULL to keep

@@ -12,20 +12,27 @@
 // Design on sm_103a (the page's GB200 kernel is prior art, not a blueprint):
 //
 //  * One CTA = one request x 16 heads x one contiguous slice of its top-k
-//    list.  Warp 4 is the producer: each lane resolves one selected row
-//    through the block table and issues one cp.async.bulk copy of the whole
-//    row (352 or 576 bytes, 16-byte aligned) into a 4-stage shared-memory
-//    ring; rows that are masked (-1, past the context, bad block id) are
-//    zero-filled instead of read.  Stage completion is an mbarrier with
-//    transaction bytes.
-//  * Warps 0-3 consume 16-row m-tiles.  Warp w owns latent dims
-//    [128w, 128w+128) and rope dims [16w, 16w+16): it unpacks only those
-//    bytes, straight into mma.sync A fragments (cvt e2m1x2 / e4m3x2 -> f16x2,
-//    times the group's e4m3 scale; the products are exact in FP16), and
-//    computes its partial Q.K^T with the 16 heads' absorbed query held in
-//    registers as B fragments.  The four partial score tiles are summed
+//    list; four warps, all of which load, unpack and compute.  At entry the
+//    CTA resolves every row of its slice (top-k index, then block table) in
+//    batches of independent loads and keeps the byte offsets in shared
+//    memory; rows that are masked (-1, past the context, logical block past
+//    the table, block id outside the pool) get offset -1.
+//  * Rows travel in stages of 32 through a ring of shared-memory slots (4
+//    for NVFP4, 3 for FP8).  Every thread issues 16-byte cp.async copies for
+//    its share of a stage (masked rows are zero-filled, nothing is read) and
+//    then arrives on the slot's mbarrier through cp.async.mbarrier.arrive, so
+//    the barrier completes when all copies of the stage have landed.  Two
+//    stages are issued up front and up to two more at each stage boundary.
+//  * Warp w owns latent dims [128w, 128w+128) and rope dims [16w, 16w+16):
+//    it unpacks only those bytes of both 16-row m-tiles, straight into
+//    mma.sync A fragments (cvt e2m1x2 / e4m3x2 -> f16x2, times the group's
+//    e4m3 scale; the products are exact in FP16), and computes its partial
+//    Q.K^T against the 16 heads' absorbed query (B fragments kept in shared
+//    memory in fragment order).  The four partial score tiles are summed
 //    through shared memory; warp w then owns the online softmax of heads
-//    [4w, 4w+4) and publishes P (f16) and the rescale factors.
+//    [4w, 4w+4) with lane = token, and publishes P (f16) and the rescale
+//    factors.  The running maximum is lazy: it is raised only when a score
+//    exceeds it by more than 2^8, so most stages need no rescale.
 //  * P.V reuses the same A fragments: the transpose of each 8x8 tile
 //    (movmatrix) is exactly the B fragment of the [tokens x dims] value
 //    operand, so every stored value is unpacked once per CTA.  Warp w keeps
@@ -36,8 +43,9 @@
 //    back in natural order.
 //  * When a request's list is split over several CTAs, each writes its
 //    normalised partial output and base-2 LSE to the workspace and a small
-//    merge kernel combines them (the pages merge in-cluster through DSMEM;
-//    this build uses a second launch).
+//    merge kernel, launched as a programmatic dependent of the decode grid,
+//    combines them (the pages merge in-cluster through distributed shared
+//    memory; this build uses a second launch).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
