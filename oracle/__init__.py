@@ -16,6 +16,10 @@ Parity status per function (pins live in ``tests/test_oracle_*.py``):
 * indexer score -- pinned (one-hot head weights against an independent
   numpy recomputation from the OCP decode table, relu / sign cases).
 * top-k -- pinned (numpy lexsort brute force, all-equal scores, ctx < k).
+* staged FP8 copy of an NVFP4 row -- pinned (nearest-e4m3 brute force over
+  the independently decoded values, exactly representable rows, saturation).
+* indexer-key quantize -- pinned (nearest-e4m3 brute force on the float
+  quotient, power-of-two scaling invariance, amax code, zero key).
 
 Sources: "Prime Inference: serving GLM-5.3 to agents is a KV-cache problem"
 (sections "Four bits per latent value" and "A kernel that reads four bits
@@ -80,6 +84,14 @@ def lib():
         L.oracle_topk_request.argtypes = [P, i32, i32, P]
         L.oracle_topk_request_f32.restype = None
         L.oracle_topk_request_f32.argtypes = [P, i32, i32, P]
+        L.oracle_stage_row_fp8.restype = None
+        L.oracle_stage_row_fp8.argtypes = [P, P]
+        L.oracle_stage_rows_fp8.restype = None
+        L.oracle_stage_rows_fp8.argtypes = [P, i64, i64, P, i32, P, P, i32, i32, i32, P, P]
+        L.oracle_quantize_index_key.restype = None
+        L.oracle_quantize_index_key.argtypes = [P, P, P]
+        L.oracle_index_key_quantize_append.restype = i64
+        L.oracle_index_key_quantize_append.argtypes = [P, P, i64, P, i64, i32, i64]
         _lib = L
     return _lib
 
@@ -164,6 +176,58 @@ def kv_quantize_append(latent, rope, slot_mapping, kv_pool: np.ndarray, num_bloc
     assert kv_pool.size >= num_blocks * kv_block_stride
     return int(lib().oracle_kv_quantize_append(_ptr(lat), _ptr(rp), _ptr(sm), n, _ptr(kv_pool), num_blocks,
                                                block_size, kv_block_stride, fmt))
+
+
+# ---------------------------------------------------------------- staged path
+def stage_row_fp8(row: np.ndarray) -> np.ndarray:
+    """One stored NVFP4 row -> the staged path's 576-byte FP8 row."""
+    r = np.ascontiguousarray(row, dtype=np.uint8).reshape(row_bytes(FMT_NVFP4))
+    out = np.zeros(row_bytes(FMT_FP8), dtype=np.uint8)
+    lib().oracle_stage_row_fp8(_ptr(r), _ptr(out))
+    return out
+
+
+def stage_rows_fp8(kv_pool, kv_block_stride, num_blocks, block_table, context_lens, topk_idx, block_size,
+                   staged_pool: np.ndarray) -> np.ndarray:
+    """Staged gather of a batch into ``staged_pool`` (uint8, in place; rows of
+    masked entries are left untouched).  Returns staged_topk int32 [B, k]:
+    j for a valid entry j, -1 for a masked one."""
+    pool = np.ascontiguousarray(kv_pool, dtype=np.uint8)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    tk = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    B, k = tk.shape
+    nblk = (k + block_size - 1) // block_size
+    assert staged_pool.dtype == np.uint8 and staged_pool.flags["C_CONTIGUOUS"]
+    assert staged_pool.size >= B * nblk * block_size * row_bytes(FMT_FP8)
+    out = np.empty((B, k), dtype=np.int32)
+    lib().oracle_stage_rows_fp8(_ptr(pool), int(kv_block_stride), int(num_blocks), _ptr(bt), bt.shape[1], _ptr(cl),
+                                _ptr(tk), B, block_size, k, _ptr(staged_pool), _ptr(out))
+    return out
+
+
+# ---------------------------------------------------------------- indexer keys
+def quantize_index_key(key_bf16) -> tuple:
+    """128 bf16 key values -> (128 e4m3 codes uint8, float32 scale)."""
+    k = np.ascontiguousarray(key_bf16, dtype=np.uint16).reshape(IDX_DIM)
+    codes = np.zeros(IDX_DIM, dtype=np.uint8)
+    sc = np.zeros(1, dtype=np.float32)
+    lib().oracle_quantize_index_key(_ptr(k), _ptr(codes), _ptr(sc))
+    return codes, sc[0]
+
+
+def index_key_quantize_append(keys, slot_mapping, key_pool: np.ndarray, num_blocks: int, block_size: int,
+                              key_block_stride: int) -> int:
+    """Indexer-key quantize-on-write into ``key_pool`` (uint8, in place);
+    returns the number of skipped tokens."""
+    k = np.ascontiguousarray(keys, dtype=np.uint16)
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    n = sm.shape[0]
+    assert k.size == n * IDX_DIM
+    assert key_pool.dtype == np.uint8 and key_pool.flags["C_CONTIGUOUS"]
+    assert key_pool.size >= num_blocks * key_block_stride
+    return int(lib().oracle_index_key_quantize_append(_ptr(k), _ptr(sm), n, _ptr(key_pool), num_blocks,
+                                                      block_size, key_block_stride))
 
 
 # ---------------------------------------------------------------- decode

@@ -44,6 +44,10 @@
  *             masked: no load and no weight (it does not enter the softmax).
  *  R-empty    a request with no valid entry outputs zeros and lse = -inf.
  *  R-keys     indexer key block = bs x 128 e4m3 bytes, then bs fp32 scales.
+ *  R-stage   the staged path's FP8 copy of an NVFP4 row holds
+ *             e4m3_rn_satfinite(e2m1 * S) per latent value, rope bytes copied.
+ *  R-keyscale indexer key scale s = amax / 448, codes e4m3(k / s), both
+ *             divisions in IEEE single precision; amax = 0 -> s = 0, codes 0.
  *  R-topk     order by (score descending, token index ascending), take the
  *             first min(k, ctx), emit them in ascending index order, pad -1.
  *             -0.0 compares equal to +0.0.
@@ -240,6 +244,52 @@ int64_t oracle_kv_quantize_append(const uint16_t* latent, const uint16_t* rope, 
 }
 
 /* ------------------------------------------------------------------------ */
+/* Staged path: NVFP4 rows re-stored as FP8 rows (ablation)                  */
+/* ------------------------------------------------------------------------ */
+
+/* One stored NVFP4 row -> the 576-byte FP8 row written by the staged path of
+ * [P1 "A kernel that reads four bits directly", figure "staged vs native
+ * decode": a gather kernel reads the 352-byte rows and writes a 576-byte FP8
+ * copy, which an FP8 attention kernel then reads].  R-stage: every latent
+ * value c_i = e2m1_i * S_g is re-encoded as e4m3 (nearest-even, satfinite,
+ * sign kept); the 64 rope bytes are e4m3 already and are copied. */
+void oracle_stage_row_fp8(const uint8_t* row, uint8_t* out) {
+  double c[ORACLE_LATENT], r[ORACLE_ROPE];
+  oracle_dequant_row(row, 0, c, r);
+  for (int i = 0; i < ORACLE_LATENT; i++) out[i] = oracle_e4m3_from_double(c[i]);
+  memcpy(out + ORACLE_ROPE_OFF_FP8, row + ORACLE_ROPE_OFF_NVFP4, ORACLE_ROPE);
+}
+
+/* Staged gather of a batch.  Entry j of request b, token t = topk_idx[b,j],
+ * is valid when 0 <= t < context_lens[b], t / bs < max_blocks_per_req and the
+ * physical block block_table[b, t / bs] lies in [0, num_blocks) (R-mask).  A
+ * valid entry writes the staged row of t at
+ *   staged_pool + ((b * nblk + j / bs) * bs + j % bs) * 576,  nblk = ceil(topk / bs)
+ * and staged_topk[b,j] = j; a masked entry writes staged_topk[b,j] = -1 and
+ * no row.  With staged block table [b,i] = b * nblk + i and staged context
+ * length nblk * bs the staged pool is an ordinary 576-byte paged pool. */
+void oracle_stage_rows_fp8(const uint8_t* kv_pool, int64_t kv_block_stride, int64_t num_blocks,
+                           const int32_t* block_table, int max_blocks_per_req, const int32_t* context_lens,
+                           const int32_t* topk_idx, int batch, int block_size, int topk, uint8_t* staged_pool,
+                           int32_t* staged_topk) {
+  int64_t nblk = (topk + block_size - 1) / block_size;
+  for (int b = 0; b < batch; b++) {
+    for (int j = 0; j < topk; j++) {
+      int t = topk_idx[(int64_t)b * topk + j];
+      int ok = t >= 0 && t < context_lens[b] && t / block_size < max_blocks_per_req;
+      int64_t blk = ok ? block_table[(int64_t)b * max_blocks_per_req + t / block_size] : -1;
+      ok = ok && blk >= 0 && blk < num_blocks;
+      staged_topk[(int64_t)b * topk + j] = ok ? j : -1;
+      if (!ok) continue;
+      const uint8_t* row = kv_pool + blk * kv_block_stride + (int64_t)(t % block_size) * ORACLE_NVFP4_ROW;
+      uint8_t* dst = staged_pool + (((int64_t)b * nblk + j / block_size) * block_size + j % block_size) *
+                                       (int64_t)ORACLE_FP8_ROW;
+      oracle_stage_row_fp8(row, dst);
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Absorbed-form sparse MLA decode, one request                              */
 /* ------------------------------------------------------------------------ */
 
@@ -348,6 +398,54 @@ void oracle_indexer_scores_request(const uint16_t* q_idx, const float* head_w, i
     }
     scores[t] = score;
   }
+}
+
+/* One token's 128 bf16 indexer-key values -> 128 e4m3 codes and a float
+ * scale [P5 section 3: 128 FP8 values plus a 4-byte scale per token].
+ * R-keyscale: s = amax / 448 and code_d = e4m3_rn_satfinite(k_d / s), both
+ * divisions in IEEE single precision (the precision of the stored scale, so
+ * every rounding decision is taken on a float).  amax = 0 stores s = 0 and
+ * 128 zero codes. */
+void oracle_quantize_index_key(const uint16_t* key, uint8_t* codes, float* scale) {
+  float amax = 0.0f;
+  for (int d = 0; d < ORACLE_IDX_DIM; d++) {
+    float x = (float)oracle_bf16_to_double(key[d]);
+    if (fabsf(x) > amax) amax = fabsf(x);
+  }
+  if (amax == 0.0f) {
+    memset(codes, 0, ORACLE_IDX_DIM);
+    *scale = 0.0f;
+    return;
+  }
+  float s = amax / 448.0f;
+  for (int d = 0; d < ORACLE_IDX_DIM; d++) {
+    float q = (float)oracle_bf16_to_double(key[d]) / s;
+    codes[d] = oracle_e4m3_from_double((double)q);
+  }
+  *scale = s;
+}
+
+/* Indexer-key quantize-on-write: token n's key goes to slot_mapping[n]
+ * (block = slot / bs, offset o = slot % bs): codes at block + o * 128, scale
+ * at block + bs * 128 + o * 4 (R-keys).  Slots that are negative or past the
+ * pool are skipped; returns their number. */
+int64_t oracle_index_key_quantize_append(const uint16_t* keys, const int64_t* slot_mapping, int64_t n_tokens,
+                                         uint8_t* key_pool, int64_t num_blocks, int block_size,
+                                         int64_t key_block_stride) {
+  int64_t skipped = 0;
+  for (int64_t n = 0; n < n_tokens; n++) {
+    int64_t slot = slot_mapping[n];
+    if (slot < 0 || slot / block_size >= num_blocks) {
+      skipped++;
+      continue;
+    }
+    uint8_t* blk = key_pool + (slot / block_size) * key_block_stride;
+    int64_t o = slot % block_size;
+    float s;
+    oracle_quantize_index_key(keys + n * ORACLE_IDX_DIM, blk + o * ORACLE_IDX_DIM, &s);
+    memcpy(blk + (int64_t)block_size * ORACLE_IDX_DIM + o * 4, &s, 4);
+  }
+  return skipped;
 }
 
 typedef struct {
