@@ -315,15 +315,20 @@ def main():
         layers.append(wl)
     ws_bytes = m.mla_sparse_decode_workspace_size(B, H, K)
     workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    # the staged path's FP8 copy is a temporary buffer that every layer reuses
+    ws_staged = torch.empty(m.mla_sparse_decode_staged_workspace_size(B, H, K), dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
 
     stream = torch.cuda.Stream(device=dev)
 
     def decode_all(fmt):
-        fn = m.mla_sparse_decode if fmt == 0 else m.mla_sparse_decode_fp8
+        # fmt 0: native NVFP4, 1: FP8 cache, 2: staged NVFP4 (gather to an FP8 copy, then the FP8 decode)
+        fn = {0: m.mla_sparse_decode, 1: m.mla_sparse_decode_fp8, 2: m.mla_sparse_decode_staged}[fmt]
+        pool_fmt = 1 if fmt == 1 else 0
+        ws = ws_staged if fmt == 2 else workspace
         for wl in layers:
-            fn(wl.q_nope, wl.q_rope, wl.pools[fmt], wl.strides[fmt], wl.num_blocks, wl.block_table,
-               wl.context_lens, wl.topk_idx, wl.softmax_scale, out=wl.out, lse=wl.lse, workspace=workspace,
+            fn(wl.q_nope, wl.q_rope, wl.pools[pool_fmt], wl.strides[pool_fmt], wl.num_blocks, wl.block_table,
+               wl.context_lens, wl.topk_idx, wl.softmax_scale, out=wl.out, lse=wl.lse, workspace=ws,
                stream=stream)
 
     def capture(fmt):
@@ -335,7 +340,7 @@ def main():
                 decode_all(fmt)
         return g
 
-    graphs = {0: capture(0), 1: capture(1)}
+    graphs = {0: capture(0), 1: capture(1), 2: capture(2)}
     torch.cuda.synchronize()
 
     def timed(g, steps, warmup):
@@ -361,12 +366,14 @@ def main():
     with ClockSampler(pci, local) as clocks:
         ms4 = timed(graphs[0], args.steps, args.warmup)
         ms8 = timed(graphs[1], args.steps, args.warmup)
+        ms_st = timed(graphs[2], args.steps, args.warmup)
     clk = clocks.summary()
     splits = m.mla_sparse_decode_workspace_size(B, H, K) > 0
     launches_per_step = L * (2 if splits else 1)
 
     per_layer4 = ms4 / L * 1e-3
     per_layer8 = ms8 / L * 1e-3
+    per_layer_st = ms_st / L * 1e-3
     rows = B * K
     value = whole_job_rate(rows, world, per_layer4)
     ach4 = layer_bytes4 / per_layer4 / 1e9
@@ -437,6 +444,12 @@ def main():
         "fp8": {"value": whole_job_rate(rows, world, per_layer8), "unit": UNIT, "per_layer_us": per_layer8 * 1e6,
                 "hbm_gbs": ach8, "frac": ach8 / hbm, "roofline_us": roof_t8 * 1e6,
                 "bytes_per_row": ROW_FP8 + 4},
+        "staged": {"value": whole_job_rate(rows, world, per_layer_st), "unit": UNIT,
+                   "per_layer_us": per_layer_st * 1e6, "vs_native": per_layer_st / per_layer4,
+                   "vs_fp8": per_layer_st / per_layer8,
+                   "bytes_per_row": ROW_NVFP4 + 4 + 2 * (ROW_FP8 + 4),
+                   "note": "gather kernel writes a 576-byte FP8 copy of each selected row into a buffer every "
+                           "layer reuses, then the FP8 decode reads it"},
         "nvfp4_bytes_per_row": ROW_NVFP4 + 4,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
@@ -478,6 +491,26 @@ def sub_measurements(m, W, dev, stream, args, hbm):
                                                "frac": bytes_ / t / 1e9 / hbm}
         del pool
     out["append"] = {"workload": wl.name, **res}
+    # indexer-key quantize-on-write of the same new tokens (the keys are
+    # seeded bf16 values, here the first 128 latent values of each token)
+    keys = wl.latent[:, :128].contiguous()
+    kstride = 64 * 132
+    kpool = torch.zeros(wl.num_blocks * kstride, dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            m.mla_index_key_quantize_append(keys, wl.slot_mapping, kpool, wl.num_blocks, 64, kstride, stream=stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            m.mla_index_key_quantize_append(keys, wl.slot_mapping, kpool, wl.num_blocks, 64, kstride, stream=stream)
+        e1.record(stream)
+    e1.synchronize()
+    t = e0.elapsed_time(e1) / args.steps * 1e-3
+    kbytes = n * (128 * 2 + 8 + 132)
+    out["index_key_append"] = {"workload": f"{n:,} new tokens' indexer keys (128 bf16 -> 128 e4m3 + float scale)",
+                               "rows_per_s": n / t, "us": t * 1e6, "hbm_gbs": kbytes / t / 1e9,
+                               "frac": kbytes / t / 1e9 / hbm}
+    del kpool, keys
     del wl
     torch.cuda.empty_cache()
 

@@ -113,6 +113,27 @@ mla_status_t mla_kv_quantize_append(const uint16_t* latent, const uint16_t* rope
                                     int64_t kv_block_stride, mla_kv_format_t fmt, mla_stream_t stream);
 
 /*
+ * Quantize-on-write of the indexer's keys ("GLM-5.3 PCP/DCP long-context on
+ * H200", section 3: 128 FP8 values plus a 4-byte scale per token).  Per
+ * token: s = max_d |k_d| / 448 and code_d = e4m3_rn_satfinite(k_d / s), both
+ * divisions IEEE float32; a key whose values are all zero stores s = 0 and
+ * 128 zero codes.  Block layout (the layout mla_indexer_topk reads): block b
+ * at idx_key_pool + b * idx_block_stride holds block_size x 128 code bytes,
+ * then block_size float scales.
+ *
+ *   keys          device bf16 [n_tokens, 128], 16-byte aligned
+ *   slot_mapping  device int64 [n_tokens]; as for mla_kv_quantize_append
+ *                 (a negative or out-of-pool slot is skipped)
+ *   idx_key_pool  device, 16-byte aligned
+ *   idx_block_stride  bytes, a multiple of 16, >= block_size * 132
+ *   block_size    64
+ * n_tokens == 0 is a no-op.  Two tokens with the same slot race.
+ */
+mla_status_t mla_index_key_quantize_append(const uint16_t* keys, const int64_t* slot_mapping, int64_t n_tokens,
+                                           void* idx_key_pool, int64_t num_blocks, int block_size,
+                                           int64_t idx_block_stride, mla_stream_t stream);
+
+/*
  * Absorbed-form sparse MLA decode over the NVFP4 cache ("Prime Inference",
  * section "A kernel that reads four bits directly").  For request b and head
  * h, with V_b = { t in topk_idx[b, :] : 0 <= t < context_lens[b] } (counted
@@ -192,6 +213,45 @@ mla_status_t mla_sparse_decode_fp8(const uint16_t* q_nope, const uint16_t* q_rop
                                    int batch, int num_heads, int block_size, int topk, float softmax_scale,
                                    uint16_t* out, float* lse, void* workspace, size_t workspace_bytes,
                                    mla_stream_t stream);
+
+/*
+ * Staged path, kept as an ablation of the native decode ("Prime Inference",
+ * section "A kernel that reads four bits directly", figure "staged vs native
+ * decode": the first version gathered the selected NVFP4 rows, wrote an FP8
+ * copy of each to GPU memory and ran the FP8 attention kernel on the copy,
+ * moving 352 + 576 + 576 bytes per selected row instead of 352).
+ *
+ * mla_stage_rows_fp8 is the gather step.  For request b and list entry j
+ * with token t = topk_idx[b, j], valid exactly when mla_sparse_decode would
+ * use it, the 576-byte FP8 row holding e4m3_rn_satfinite(e2m1 x S) for each
+ * latent value and the row's 64 rope bytes unchanged is written at
+ *   staged_pool + (b * nblk * 64 + j) * 576,   nblk = ceil(topk / 64),
+ * and staged_topk[b, j] = j; a masked entry writes staged_topk[b, j] = -1
+ * and no row.  With block table [b, i] = b * nblk + i and context length
+ * nblk * 64, the staged pool is an ordinary FP8 pool (block stride
+ * 64 * 576) for mla_sparse_decode_fp8 with staged_topk as its list.
+ *
+ *   kv_pool ... topk   as for mla_sparse_decode (NVFP4 pool)
+ *   staged_pool   device, 16-byte aligned, mla_staged_pool_bytes(batch, topk)
+ *   staged_topk   device int32 [batch, topk]
+ *
+ * mla_sparse_decode_staged runs both steps (the gather, then the FP8 decode)
+ * with every intermediate in `workspace`; its arguments and results are those
+ * of mla_sparse_decode, and its outputs differ from the native decode's only
+ * by the e4m3 rounding of the staged copy.
+ */
+size_t mla_staged_pool_bytes(int batch, int topk);
+mla_status_t mla_stage_rows_fp8(const void* kv_pool, int64_t kv_block_stride, int64_t num_blocks,
+                                const int32_t* block_table, int max_blocks_per_req, const int32_t* context_lens,
+                                const int32_t* topk_idx, int batch, int block_size, int topk, void* staged_pool,
+                                int32_t* staged_topk, mla_stream_t stream);
+size_t mla_sparse_decode_staged_workspace_size(int batch, int num_heads, int topk);
+mla_status_t mla_sparse_decode_staged(const uint16_t* q_nope, const uint16_t* q_rope, const void* kv_pool,
+                                      int64_t kv_block_stride, int64_t num_blocks, const int32_t* block_table,
+                                      int max_blocks_per_req, const int32_t* context_lens, const int32_t* topk_idx,
+                                      int batch, int num_heads, int block_size, int topk, float softmax_scale,
+                                      uint16_t* out, float* lse, void* workspace, size_t workspace_bytes,
+                                      mla_stream_t stream);
 
 /*
  * Exact top-k over float scores ("GLM-5.3 PCP/DCP long-context on H200",

@@ -173,7 +173,7 @@ def kv_quantize_append(latent, rope, slot_mapping, kv_pool: np.ndarray, num_bloc
     n = sm.shape[0]
     assert lat.size == n * LATENT and rp.size == n * ROPE
     assert kv_pool.dtype == np.uint8 and kv_pool.flags["C_CONTIGUOUS"]
-    assert kv_pool.size >= num_blocks * kv_block_stride
+    assert num_blocks == 0 or kv_pool.size >= (num_blocks - 1) * kv_block_stride + block_size * row_bytes(fmt)
     return int(lib().oracle_kv_quantize_append(_ptr(lat), _ptr(rp), _ptr(sm), n, _ptr(kv_pool), num_blocks,
                                                block_size, kv_block_stride, fmt))
 
@@ -225,7 +225,7 @@ def index_key_quantize_append(keys, slot_mapping, key_pool: np.ndarray, num_bloc
     n = sm.shape[0]
     assert k.size == n * IDX_DIM
     assert key_pool.dtype == np.uint8 and key_pool.flags["C_CONTIGUOUS"]
-    assert key_pool.size >= num_blocks * key_block_stride
+    assert num_blocks == 0 or key_pool.size >= (num_blocks - 1) * key_block_stride + block_size * (IDX_DIM + 4)
     return int(lib().oracle_index_key_quantize_append(_ptr(k), _ptr(sm), n, _ptr(key_pool), num_blocks,
                                                       block_size, key_block_stride))
 

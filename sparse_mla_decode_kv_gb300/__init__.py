@@ -19,7 +19,9 @@ __all__ = [
     "mla_kv_row_bytes", "mla_status_string", "mla_last_cuda_error", "mla_device_fault",
     "mla_kv_quantize_append", "mla_sparse_decode_workspace_size", "mla_sparse_decode",
     "mla_sparse_decode_fp8", "mla_sparse_decode_noalloc", "mla_topk_workspace_size", "mla_topk",
-    "mla_indexer_topk_workspace_size", "mla_indexer_topk",
+    "mla_indexer_topk_workspace_size", "mla_indexer_topk", "mla_index_key_quantize_append",
+    "mla_staged_pool_bytes", "mla_stage_rows_fp8", "mla_sparse_decode_staged_workspace_size",
+    "mla_sparse_decode_staged",
 ]
 
 MLA_KV_NVFP4 = 0
@@ -51,6 +53,12 @@ SIGNATURES = {
     "mla_indexer_topk_workspace_size": (_SZ, [_I32, _I32, _I32]),
     "mla_indexer_topk": (_I32, [_P, _P, _P, _I64, _I64, _P, _I32, _P, _I32, _I32, _I32, _I32, _P, _P, _I32, _P,
                                 _SZ, _P]),
+    "mla_index_key_quantize_append": (_I32, [_P, _P, _I64, _P, _I64, _I32, _I64, _P]),
+    "mla_staged_pool_bytes": (_SZ, [_I32, _I32]),
+    "mla_stage_rows_fp8": (_I32, [_P, _I64, _I64, _P, _I32, _P, _P, _I32, _I32, _I32, _P, _P, _P]),
+    "mla_sparse_decode_staged_workspace_size": (_SZ, [_I32, _I32, _I32]),
+    "mla_sparse_decode_staged": (_I32, [_P, _P, _P, _I64, _I64, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _F32, _P,
+                                        _P, _P, _SZ, _P]),
 }
 
 
@@ -151,11 +159,28 @@ def mla_kv_quantize_append(latent: torch.Tensor, rope: torch.Tensor, slot_mappin
     n = slot_mapping.numel()
     if latent.numel() != n * 512 or rope.numel() != n * 64:
         raise ValueError("latent must be [n,512] and rope [n,64] for n = len(slot_mapping)")
-    if kv_pool.numel() * kv_pool.element_size() < num_blocks * kv_block_stride:
-        raise ValueError("kv_pool is smaller than num_blocks * kv_block_stride")
+    if num_blocks > 0 and kv_pool.numel() * kv_pool.element_size() < (num_blocks - 1) * kv_block_stride + \
+            block_size * (352 if fmt == MLA_KV_NVFP4 else 576):
+        raise ValueError("kv_pool does not reach the last row of block num_blocks - 1")
     _check("mla_kv_quantize_append",
            load().mla_kv_quantize_append(_ptr(latent), _ptr(rope), _ptr(slot_mapping), n, _ptr(kv_pool),
                                          num_blocks, block_size, kv_block_stride, fmt, _stream(stream)))
+
+
+def mla_index_key_quantize_append(keys: torch.Tensor, slot_mapping: torch.Tensor, idx_key_pool: torch.Tensor,
+                                  num_blocks: int, block_size: int, idx_block_stride: int, stream=None) -> None:
+    """Indexer keys bf16 [n, 128] -> 128 e4m3 codes + a float scale per token, by slot."""
+    keys = _bits(keys, "keys")
+    slot_mapping = _contig(slot_mapping, torch.int64, "slot_mapping")
+    n = slot_mapping.numel()
+    if keys.numel() != n * 128:
+        raise ValueError("keys must be [n,128] for n = len(slot_mapping)")
+    if num_blocks > 0 and idx_key_pool.numel() * idx_key_pool.element_size() < (num_blocks - 1) * idx_block_stride + \
+            block_size * 132:
+        raise ValueError("idx_key_pool does not reach the last scale of block num_blocks - 1")
+    _check("mla_index_key_quantize_append",
+           load().mla_index_key_quantize_append(_ptr(keys), _ptr(slot_mapping), n, _ptr(idx_key_pool), num_blocks,
+                                                block_size, idx_block_stride, _stream(stream)))
 
 
 # --------------------------------------------------------------------- sparse decode
@@ -164,7 +189,8 @@ def mla_sparse_decode_workspace_size(batch: int, num_heads: int, topk: int) -> i
 
 
 def _decode(cname: str, q_nope, q_rope, kv_pool, kv_block_stride, num_blocks, block_table, context_lens, topk_idx,
-            softmax_scale, block_size=64, out=None, lse=None, workspace=None, stream=None):
+            softmax_scale, block_size=64, out=None, lse=None, workspace=None, stream=None,
+            ws_size=mla_sparse_decode_workspace_size):
     q_nope = _bits(q_nope, "q_nope")
     q_rope = _bits(q_rope, "q_rope")
     block_table = _contig(block_table, torch.int32, "block_table")
@@ -174,7 +200,7 @@ def _decode(cname: str, q_nope, q_rope, kv_pool, kv_block_stride, num_blocks, bl
     topk = topk_idx.shape[1]
     if out is None:
         out = torch.empty((batch, heads, 512), dtype=torch.bfloat16, device=q_nope.device)
-    need = mla_sparse_decode_workspace_size(batch, heads, topk)
+    need = ws_size(batch, heads, topk)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q_nope.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -197,6 +223,44 @@ def mla_sparse_decode_fp8(q_nope, q_rope, kv_pool, kv_block_stride, num_blocks, 
     """FP8 (576-byte) cache.  Returns (out bf16 [B,H,512], lse or None)."""
     return _decode("mla_sparse_decode_fp8", q_nope, q_rope, kv_pool, kv_block_stride, num_blocks, block_table,
                    context_lens, topk_idx, softmax_scale, block_size, out, lse, workspace, stream)
+
+
+def mla_sparse_decode_staged_workspace_size(batch: int, num_heads: int, topk: int) -> int:
+    return int(load().mla_sparse_decode_staged_workspace_size(batch, num_heads, topk))
+
+
+def mla_sparse_decode_staged(q_nope, q_rope, kv_pool, kv_block_stride, num_blocks, block_table, context_lens,
+                             topk_idx, softmax_scale, block_size=64, out=None, lse=None, workspace=None, stream=None):
+    """Staged path over the NVFP4 cache (gather to an FP8 copy, then the FP8
+    decode).  Returns (out bf16 [B,H,512], lse or None)."""
+    return _decode("mla_sparse_decode_staged", q_nope, q_rope, kv_pool, kv_block_stride, num_blocks, block_table,
+                   context_lens, topk_idx, softmax_scale, block_size, out, lse, workspace, stream,
+                   ws_size=mla_sparse_decode_staged_workspace_size)
+
+
+def mla_staged_pool_bytes(batch: int, topk: int) -> int:
+    return int(load().mla_staged_pool_bytes(batch, topk))
+
+
+def mla_stage_rows_fp8(kv_pool, kv_block_stride, num_blocks, block_table, context_lens, topk_idx, block_size=64,
+                       staged_pool=None, staged_topk=None, stream=None):
+    """Gather step of the staged path.  Returns (staged_pool uint8, staged_topk int32 [B, topk])."""
+    block_table = _contig(block_table, torch.int32, "block_table")
+    context_lens = _contig(context_lens, torch.int32, "context_lens")
+    topk_idx = _contig(topk_idx, torch.int32, "topk_idx")
+    batch, topk = topk_idx.shape
+    dev = topk_idx.device
+    if staged_pool is None:
+        staged_pool = torch.empty(mla_staged_pool_bytes(batch, topk), dtype=torch.uint8, device=dev)
+    if staged_pool.numel() * staged_pool.element_size() < mla_staged_pool_bytes(batch, topk):
+        raise ValueError("staged_pool is smaller than mla_staged_pool_bytes(batch, topk)")
+    if staged_topk is None:
+        staged_topk = torch.empty((batch, topk), dtype=torch.int32, device=dev)
+    _check("mla_stage_rows_fp8",
+           load().mla_stage_rows_fp8(_ptr(kv_pool), kv_block_stride, num_blocks, _ptr(block_table),
+                                     block_table.shape[1], _ptr(context_lens), _ptr(topk_idx), batch, block_size,
+                                     topk, _ptr(staged_pool), _ptr(staged_topk), _stream(stream)))
+    return staged_pool, staged_topk
 
 
 def mla_sparse_decode_noalloc(q_nope, q_rope, kv_pool, kv_block_stride, num_blocks, block_table, context_lens,

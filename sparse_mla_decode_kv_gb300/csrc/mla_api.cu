@@ -193,6 +193,103 @@ mla_status_t mla_sparse_decode_fp8(const uint16_t* q_nope, const uint16_t* q_rop
                      out, lse, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
+mla_status_t mla_index_key_quantize_append(const uint16_t* keys, const int64_t* slot_mapping, int64_t n_tokens,
+                                           void* idx_key_pool, int64_t num_blocks, int block_size,
+                                           int64_t idx_block_stride, mla_stream_t stream) {
+  if (n_tokens < 0 || num_blocks < 0) return MLA_ERR_INVALID_ARG;
+  mla_status_t s = check_block_size(block_size);
+  if (s != MLA_OK) return s;
+  if (idx_block_stride % 16 != 0 || idx_block_stride < static_cast<int64_t>(block_size) * (kIdxDim + 4))
+    return MLA_ERR_INVALID_ARG;
+  if (n_tokens == 0) return MLA_OK;
+  if (!keys || !slot_mapping || !idx_key_pool) return MLA_ERR_INVALID_ARG;
+  if (!aligned(keys, 16) || !aligned(slot_mapping, 8) || !aligned(idx_key_pool, 16)) return MLA_ERR_INVALID_ARG;
+  return cuda_status(launch_index_key_append(keys, slot_mapping, n_tokens, idx_key_pool, num_blocks,
+                                             idx_block_stride, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t mla_staged_pool_bytes(int batch, int topk) {
+  if (batch <= 0 || topk < 1) return 0;
+  const int64_t nblk = (topk + kBlock - 1) / kBlock;
+  return static_cast<size_t>(batch) * nblk * kBlock * kRowFp8;
+}
+
+mla_status_t mla_stage_rows_fp8(const void* kv_pool, int64_t kv_block_stride, int64_t num_blocks,
+                                const int32_t* block_table, int max_blocks_per_req, const int32_t* context_lens,
+                                const int32_t* topk_idx, int batch, int block_size, int topk, void* staged_pool,
+                                int32_t* staged_topk, mla_stream_t stream) {
+  if (batch < 0 || topk < 1 || topk > 2048) return MLA_ERR_INVALID_ARG;
+  mla_status_t s = check_block_size(block_size);
+  if (s != MLA_OK) return s;
+  if (batch == 0) return MLA_OK;
+  if (!kv_pool || !block_table || !context_lens || !topk_idx || !staged_pool || !staged_topk)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned(kv_pool, 16) || !aligned(staged_pool, 16) || !aligned(block_table, 4) ||
+      !aligned(context_lens, 4) || !aligned(topk_idx, 4) || !aligned(staged_topk, 4))
+    return MLA_ERR_INVALID_ARG;
+  if (num_blocks < 0 || max_blocks_per_req < 1) return MLA_ERR_INVALID_ARG;
+  if (kv_block_stride % 16 != 0 || kv_block_stride < static_cast<int64_t>(block_size) * kRowNvfp4)
+    return MLA_ERR_INVALID_ARG;
+  return cuda_status(launch_stage_rows_fp8(kv_pool, kv_block_stride, num_blocks, block_table, max_blocks_per_req,
+                                           context_lens, topk_idx, batch, topk, staged_pool, staged_topk, nullptr,
+                                           nullptr, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+// Workspace of the staged decode: staged rows | staged list | identity block
+// table | context lengths | the FP8 decode's own split-K workspace.
+struct StagedLayout {
+  size_t rows, list, table, ctx, decode, total;
+};
+StagedLayout staged_layout(int batch, int num_heads, int topk) {
+  StagedLayout l{};
+  const int64_t nblk = (topk + kBlock - 1) / kBlock;
+  l.rows = align256(mla_staged_pool_bytes(batch, topk));
+  l.list = align256(static_cast<size_t>(batch) * topk * sizeof(int32_t));
+  l.table = align256(static_cast<size_t>(batch) * nblk * sizeof(int32_t));
+  l.ctx = align256(static_cast<size_t>(batch) * sizeof(int32_t));
+  l.decode = align256(plan_sparse_decode(batch, num_heads, topk).workspace);
+  l.total = l.rows + l.list + l.table + l.ctx + l.decode;
+  return l;
+}
+}  // namespace
+
+size_t mla_sparse_decode_staged_workspace_size(int batch, int num_heads, int topk) {
+  if (batch <= 0 || num_heads < 16 || num_heads % 16 != 0 || topk < 1) return 0;
+  return staged_layout(batch, num_heads, topk).total;
+}
+
+mla_status_t mla_sparse_decode_staged(const uint16_t* q_nope, const uint16_t* q_rope, const void* kv_pool,
+                                      int64_t kv_block_stride, int64_t num_blocks, const int32_t* block_table,
+                                      int max_blocks_per_req, const int32_t* context_lens, const int32_t* topk_idx,
+                                      int batch, int num_heads, int block_size, int topk, float softmax_scale,
+                                      uint16_t* out, float* lse, void* workspace, size_t workspace_bytes,
+                                      mla_stream_t stream) {
+  mla_status_t s = check_decode_args(q_nope, q_rope, kv_pool, kv_block_stride, num_blocks, block_table,
+                                     max_blocks_per_req, context_lens, topk_idx, batch, num_heads, block_size, topk,
+                                     softmax_scale, out, MLA_KV_NVFP4);
+  if (s != MLA_OK || batch == 0) return s;
+  if (lse && !aligned(lse, 4)) return MLA_ERR_INVALID_ARG;
+  const StagedLayout l = staged_layout(batch, num_heads, topk);
+  if (workspace_bytes < l.total) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  if (!workspace || !aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint8_t* rows = ws;
+  int32_t* list = reinterpret_cast<int32_t*>(ws + l.rows);
+  int32_t* table = reinterpret_cast<int32_t*>(ws + l.rows + l.list);
+  int32_t* ctx = reinterpret_cast<int32_t*>(ws + l.rows + l.list + l.table);
+  void* dec_ws = ws + l.rows + l.list + l.table + l.ctx;
+  const int nblk = (topk + kBlock - 1) / kBlock;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_stage_rows_fp8(kv_pool, kv_block_stride, num_blocks, block_table, max_blocks_per_req,
+                                        context_lens, topk_idx, batch, topk, rows, list, table, ctx, st);
+  if (e != cudaSuccess) return cuda_status(e);
+  const DecodePlan plan = plan_sparse_decode(batch, num_heads, topk);
+  return cuda_status(launch_sparse_decode(MLA_KV_FP8, q_nope, q_rope, rows, static_cast<int64_t>(kBlock) * kRowFp8,
+                                          static_cast<int64_t>(batch) * nblk, table, nblk, ctx, list, batch,
+                                          num_heads, topk, softmax_scale, out, lse, dec_ws, plan, st));
+}
+
 size_t mla_topk_workspace_size(int batch, int max_context_len, int topk) {
   if (batch <= 0 || max_context_len < 0 || topk < 1) return 0;
   return topk_workspace_bytes(batch, max_context_len, topk);

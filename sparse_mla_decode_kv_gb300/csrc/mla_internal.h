@@ -17,6 +17,16 @@ cudaError_t launch_quantize_append(const uint16_t* latent, const uint16_t* rope,
                                    int64_t n_tokens, void* pool, int64_t num_blocks, int64_t block_stride, int fmt,
                                    cudaStream_t stream);
 
+cudaError_t launch_index_key_append(const uint16_t* keys, const int64_t* slot_mapping, int64_t n_tokens, void* pool,
+                                    int64_t num_blocks, int64_t block_stride, cudaStream_t stream);
+
+// Staged path: NVFP4 rows re-stored as FP8 rows (staged_bt / staged_ctx may be
+// null; when given, the identity block table and context lengths are written).
+cudaError_t launch_stage_rows_fp8(const void* pool, int64_t block_stride, int64_t num_blocks,
+                                  const int32_t* block_table, int max_blocks_per_req, const int32_t* context_lens,
+                                  const int32_t* topk_idx, int batch, int topk, void* staged, int32_t* staged_topk,
+                                  int32_t* staged_bt, int32_t* staged_ctx, cudaStream_t stream);
+
 // Sparse decode: split plan and launch.
 struct DecodePlan {
   int splits;          // CTAs per (request, 16-head group) along the top-k list

@@ -11,6 +11,9 @@
 // with fully used 16-byte loads and writes the 352 (or 576) output bytes as
 // contiguous 8-, 1- and 2-byte lanes.  The kernel is HBM-bound: 1,160 bytes
 // in (latent + rope + slot) and 352 out per token.
+//
+// The indexer's keys have their own quantize-on-write below (128 e4m3 values
+// and a float scale per token).
 #include "mla_device.cuh"
 #include "mla_internal.h"
 
@@ -76,7 +79,71 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   }
 }
 
+// Indexer keys ("GLM-5.3 PCP/DCP long-context on H200", section 3: 128 FP8
+// values plus a 4-byte scale per token): s = amax / 448 and codes
+// e4m3(k / s), both divisions IEEE single precision; a zero key stores s = 0
+// and zero codes.  Half a warp per token: lane l of the half owns values
+// [8l, 8l+8) (one 16-byte load, one 8-byte store); the amax is a 16-lane
+// shuffle reduction.  Block layout: 64 x 128 code bytes, then 64 floats.
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+    index_key_append_kernel(const uint16_t* __restrict__ keys, const int64_t* __restrict__ slot_mapping,
+                            int64_t n_tokens, uint8_t* __restrict__ pool, int64_t num_blocks,
+                            int64_t block_stride) {
+  const int lane = threadIdx.x & 31;
+  const int half = lane >> 4;
+  const int l16 = lane & 15;
+  const int64_t warp_global = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int64_t warp_stride = static_cast<int64_t>(gridDim.x) * kWarpsPerBlock;
+  for (int64_t pair = warp_global; 2 * pair < n_tokens; pair += warp_stride) {
+    const int64_t n = 2 * pair + half;
+    const bool in_range = n < n_tokens;
+    const int64_t slot = in_range ? __ldg(slot_mapping + n) : -1;
+    const bool ok = slot >= 0 && slot / kBlock < num_blocks;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (ok) v = __ldg(reinterpret_cast<const uint4*>(keys + n * kIdxDim) + l16);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float x[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
+      x[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+    if (!ok) continue;
+    const float s = amax == 0.f ? 0.f : __fdiv_rn(amax, 448.0f);
+    uint32_t lo = 0, hi = 0;
+    if (amax != 0.f) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        lo |= f32x2_to_e4m3x2(__fdiv_rn(x[2 * i + 1], s), __fdiv_rn(x[2 * i], s)) << (16 * i);
+        hi |= f32x2_to_e4m3x2(__fdiv_rn(x[4 + 2 * i + 1], s), __fdiv_rn(x[4 + 2 * i], s)) << (16 * i);
+      }
+    }
+    uint8_t* blk = pool + (slot / kBlock) * block_stride;
+    const int64_t o = slot % kBlock;
+    *reinterpret_cast<uint2*>(blk + o * kIdxDim + 8 * l16) = make_uint2(lo, hi);
+    if (l16 == 0) *reinterpret_cast<float*>(blk + static_cast<int64_t>(kBlock) * kIdxDim + 4 * o) = s;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_index_key_append(const uint16_t* keys, const int64_t* slot_mapping, int64_t n_tokens, void* pool,
+                                    int64_t num_blocks, int64_t block_stride, cudaStream_t stream) {
+  if (n_tokens <= 0) return cudaSuccess;
+  const int64_t pairs = (n_tokens + 1) / 2;
+  int64_t want = (pairs + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
+  const int grid = static_cast<int>(want < cap ? want : cap);
+  index_key_append_kernel<<<grid, kWarpsPerBlock * 32, 0, stream>>>(keys, slot_mapping, n_tokens,
+                                                                     static_cast<uint8_t*>(pool), num_blocks,
+                                                                     block_stride);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quantize_append(const uint16_t* latent, const uint16_t* rope, const int64_t* slot_mapping,
                                    int64_t n_tokens, void* pool, int64_t num_blocks, int64_t block_stride, int fmt,

@@ -117,3 +117,42 @@ def test_workspace_sizes_are_zero_for_empty_or_invalid(lib):
     assert lib.mla_sparse_decode_workspace_size(0, 16, 2048) == 0
     assert lib.mla_sparse_decode_workspace_size(4, 8, 2048) == 0
     assert lib.mla_topk_workspace_size(0, 10, 10) == 0
+
+
+def test_index_key_append_validation(lib):
+    f = lib.mla_index_key_quantize_append
+    assert f(FAKE, FAKE, 10, FAKE, 4, 64, 64 * 132 - 16, None) == 1   # stride too small
+    assert f(FAKE, FAKE, 10, FAKE, 4, 64, 64 * 132 + 8, None) == 1    # stride not a multiple of 16
+    assert f(FAKE, FAKE, 10, FAKE, 4, 32, 32 * 132, None) == 2        # block size unsupported
+    assert f(None, FAKE, 10, FAKE, 4, 64, 64 * 132, None) == 1
+    assert f(C.c_void_p(0x10008), FAKE, 10, FAKE, 4, 64, 64 * 132, None) == 1  # keys misaligned
+    assert f(None, None, 0, None, 4, 64, 64 * 132, None) == 0         # n_tokens == 0 is a no-op
+    assert f(FAKE, FAKE, -2, FAKE, 4, 64, 64 * 132, None) == 1
+
+
+def test_staged_path_validation_and_sizes(lib):
+    assert lib.mla_staged_pool_bytes(3, 70) == 3 * 2 * 64 * 576
+    assert lib.mla_staged_pool_bytes(0, 70) == 0
+    f = lib.mla_stage_rows_fp8
+    args = [FAKE, 64 * 352, 10, FAKE, 4, FAKE, FAKE, 2, 64, 2048, FAKE, FAKE, None]
+    for i, v, want in [(0, None, 1), (10, None, 1), (11, None, 1), (1, 64 * 352 - 16, 1), (8, 32, 2),
+                       (9, 0, 1), (9, 2049, 1), (10, C.c_void_p(0x10008), 1), (4, 0, 1)]:
+        a = list(args)
+        a[i] = v
+        assert f(*a) == want, (i, v)
+    empty = list(args)
+    empty[7] = 0
+    empty[0] = None
+    assert f(*empty) == 0
+    # the staged decode validates like mla_sparse_decode, then wants its workspace
+    need = lib.mla_sparse_decode_staged_workspace_size(2, 16, 2048)
+    assert need >= lib.mla_staged_pool_bytes(2, 2048) + 2 * 2048 * 4
+    g = lib.mla_sparse_decode_staged
+    base = [FAKE, FAKE, FAKE, 64 * 352, 10, FAKE, 4, FAKE, FAKE, 2, 16, 64, 2048, 0.07, FAKE, None, None, 0, None]
+    assert g(*base) == 3
+    bad = list(base)
+    bad[10] = 24
+    assert g(*bad) == 1
+    bad = list(base)
+    bad[3] = 64 * 352 - 16  # stride too small for 352-byte rows
+    assert g(*bad) == 1

@@ -233,3 +233,35 @@ def test_softmax_scale_and_query_scaling_agree(fmt):
     o2, l2 = cache.decode(bf16(2 * qn_f), bf16(2 * qr_f), idx, 0.01)
     assert np.allclose(o1, o2, rtol=1e-12, atol=1e-14)
     assert np.allclose(l1, l2, rtol=1e-12)
+
+
+def test_block_major_pool_slices_match_packed_pools(fmt):
+    """Block-major pool ("Prime Inference", section "Moving the cache: 32K
+    copies for one request", KV layout figure): layer l's rows live at
+    l * 64 * row_bytes inside each block, block stride layers * 64 *
+    row_bytes.  Appending into one layer's slice leaves the others untouched,
+    and decoding a slice equals decoding a packed single-layer pool."""
+    rng = np.random.default_rng(21)
+    layers, ctx, nb = 3, 150, 4
+    rb = O.row_bytes(fmt)
+    sl = BS * rb
+    stride = layers * sl
+    bt = rng.permutation(nb)[:3].astype(np.int32)[None, :]
+    slots = np.array([bt[0, t // BS] * BS + t % BS for t in range(ctx)], dtype=np.int64)
+    pool = np.full(nb * stride, 0xEE, dtype=np.uint8)
+    qn, qr = rand_q(4, seed=22)
+    idx = rng.choice(ctx, 40, replace=False).astype(np.int32)[None, :]
+    cl = np.array([ctx], dtype=np.int32)
+    for layer in range(layers):
+        lat = bf16(rng.standard_normal((ctx, 512)))
+        rope = bf16(rng.standard_normal((ctx, 64)))
+        view = pool[layer * sl:]
+        O.kv_quantize_append(lat, rope, slots, view, nb, BS, stride, fmt)
+        blocks = pool.reshape(nb, layers, sl)
+        assert np.all(blocks[:, layer + 1:] == 0xEE), "later layers untouched"
+        packed = np.full(nb * sl, 0xEE, dtype=np.uint8)
+        O.kv_quantize_append(lat, rope, slots, packed, nb, BS, sl, fmt)
+        assert np.array_equal(blocks[:, layer].reshape(-1), packed)
+        a = O.sparse_decode(qn[None], qr[None], view, stride, bt, cl, idx, BS, 0.05, fmt)
+        b = O.sparse_decode(qn[None], qr[None], packed, sl, bt, cl, idx, BS, 0.05, fmt)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
