@@ -16,6 +16,9 @@ Parity status per function (pins live in ``tests/test_oracle_*.py``):
 * indexer score -- pinned (one-hot head weights against an independent
   numpy recomputation from the OCP decode table, relu / sign cases).
 * top-k -- pinned (numpy lexsort brute force, all-equal scores, ctx < k).
+* several query tokens per request -- pinned (one token equals the single-
+  token decode; the last token sees the whole context; causal masking
+  against a brute-force softmax over the explicitly visible positions).
 * staged FP8 copy of an NVFP4 row -- pinned (nearest-e4m3 brute force over
   the independently decoded values, exactly representable rows, saturation).
 * indexer-key quantize -- pinned (nearest-e4m3 brute force on the float
@@ -84,6 +87,8 @@ def lib():
         L.oracle_topk_request.argtypes = [P, i32, i32, P]
         L.oracle_topk_request_f32.restype = None
         L.oracle_topk_request_f32.argtypes = [P, i32, i32, P]
+        L.oracle_sparse_decode_mtp.restype = None
+        L.oracle_sparse_decode_mtp.argtypes = [P, P, P, i64, P, i32, P, P, i32, i32, i32, i32, i32, f64, i32, P, P]
         L.oracle_stage_row_fp8.restype = None
         L.oracle_stage_row_fp8.argtypes = [P, P]
         L.oracle_stage_rows_fp8.restype = None
@@ -261,6 +266,37 @@ def sparse_decode(q_nope, q_rope, kv_pool, kv_block_stride, block_table, context
                                        _ptr(bt[b]), int(cl[b]), _ptr(tk[b]), k, H, block_size,
                                        float(softmax_scale), fmt, o.ctypes.data_as(C.c_void_p),
                                        l.ctypes.data_as(C.c_void_p))
+
+    _run(one, len(reqs), threads)
+    return out, lse
+
+
+def sparse_decode_mtp(q_nope, q_rope, kv_pool, kv_block_stride, block_table, context_lens, topk_idx,
+                      block_size: int, softmax_scale: float, fmt: int, requests=None, threads: int = 1):
+    """Float64 decode of Q query tokens per request, each with its own top-k
+    list; token i of request b sees positions < context_lens[b] - (Q-1-i).
+
+    q_nope uint16 [B,Q,H,512], q_rope [B,Q,H,64], topk_idx int32 [B,Q,k].
+    Returns (out [R,Q,H,512], lse [R,Q,H]) for the R requests in ``requests``."""
+    qn = np.ascontiguousarray(q_nope, dtype=np.uint16)
+    qr = np.ascontiguousarray(q_rope, dtype=np.uint16)
+    pool = np.ascontiguousarray(kv_pool, dtype=np.uint8)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    tk = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    B, Q, H = qn.shape[0], qn.shape[1], qn.shape[2]
+    k = tk.shape[2]
+    reqs = list(range(B)) if requests is None else list(requests)
+    out = np.zeros((len(reqs), Q, H, LATENT), dtype=np.float64)
+    lse = np.zeros((len(reqs), Q, H), dtype=np.float64)
+    L = lib()
+
+    def one(j):
+        b = reqs[j]
+        L.oracle_sparse_decode_mtp(_ptr(qn[b]), _ptr(qr[b]), _ptr(pool), int(kv_block_stride), _ptr(bt[b]),
+                                   bt.shape[1], _ptr(cl[b:b + 1]), _ptr(tk[b]), 1, Q, H, block_size, k,
+                                   float(softmax_scale), fmt, out[j].ctypes.data_as(C.c_void_p),
+                                   lse[j].ctypes.data_as(C.c_void_p))
 
     _run(one, len(reqs), threads)
     return out, lse

@@ -44,6 +44,8 @@
  *             masked: no load and no weight (it does not enter the softmax).
  *  R-empty    a request with no valid entry outputs zeros and lse = -inf.
  *  R-keys     indexer key block = bs x 128 e4m3 bytes, then bs fp32 scales.
+ *  R-causal  with Q query tokens per request, token i is the (Q-1-i)-th
+ *             last position: it sees t < context_len - (Q - 1 - i).
  *  R-stage   the staged path's FP8 copy of an NVFP4 row holds
  *             e4m3_rn_satfinite(e2m1 * S) per latent value, rope bytes copied.
  *  R-keyscale indexer key scale s = amax / 448, codes e4m3(k / s), both
@@ -366,6 +368,30 @@ void oracle_sparse_decode(const uint16_t* q_nope, const uint16_t* q_rope, const 
                                  block_table + (size_t)b * max_blocks_per_req, context_lens[b],
                                  topk_idx + (size_t)b * topk, topk, num_heads, block_size, softmax_scale, fmt,
                                  out + (size_t)b * num_heads * ORACLE_LATENT, lse + (size_t)b * num_heads);
+}
+
+/* Several query tokens per request (speculative drafts decoded together):
+ * q_nope [B,Q,H,512], q_rope [B,Q,H,64], topk_idx [B,Q,k], out [B,Q,H,512],
+ * lse [B,Q,H].  Every query token has its own top-k list ([P1] "A kernel
+ * that reads four bits directly": the native kernel runs 15 query tokens per
+ * launch).  R-causal: the Q tokens are the last Q positions of the request's
+ * context_lens[b] tokens, so token i sees positions t < context_lens[b] -
+ * (Q - 1 - i); list entries at or past that bound are masked (R-mask). */
+void oracle_sparse_decode_mtp(const uint16_t* q_nope, const uint16_t* q_rope, const uint8_t* kv_pool,
+                              int64_t kv_block_stride, const int32_t* block_table, int max_blocks_per_req,
+                              const int32_t* context_lens, const int32_t* topk_idx, int batch, int q_len,
+                              int num_heads, int block_size, int topk, double softmax_scale, int fmt, double* out,
+                              double* lse) {
+  for (int b = 0; b < batch; b++) {
+    for (int i = 0; i < q_len; i++) {
+      int64_t v = (int64_t)b * q_len + i;
+      int ctx_i = context_lens[b] - (q_len - 1 - i);
+      oracle_sparse_decode_request(q_nope + v * num_heads * ORACLE_LATENT, q_rope + v * num_heads * ORACLE_ROPE,
+                                   kv_pool, kv_block_stride, block_table + (int64_t)b * max_blocks_per_req,
+                                   ctx_i, topk_idx + v * topk, topk, num_heads, block_size, softmax_scale, fmt,
+                                   out + v * num_heads * ORACLE_LATENT, lse + v * num_heads);
+    }
+  }
 }
 
 /* ------------------------------------------------------------------------ */

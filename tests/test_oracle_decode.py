@@ -265,3 +265,53 @@ def test_block_major_pool_slices_match_packed_pools(fmt):
         a = O.sparse_decode(qn[None], qr[None], view, stride, bt, cl, idx, BS, 0.05, fmt)
         b = O.sparse_decode(qn[None], qr[None], packed, sl, bt, cl, idx, BS, 0.05, fmt)
         assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_draft_tokens_single_token_and_causal_bounds(fmt):
+    """Q query tokens per request, each with its own list (R-causal: token i
+    sees positions < ctx - (Q - 1 - i)).  Q = 1 is the single-token decode;
+    the last token sees the whole context; the first token with the same
+    list equals the single-token decode at ctx - (Q - 1)."""
+    cache = Cache(260, fmt, seed=31)
+    rng = np.random.default_rng(32)
+    Q, H, k = 3, 4, 50
+    qn = np.stack([rand_q(H, seed=40 + i)[0] for i in range(Q)])
+    qr = np.stack([rand_q(H, seed=40 + i)[1] for i in range(Q)])
+    lst = np.concatenate([rng.choice(255, k - 5, replace=False), [255, 256, 257, 258, 259]]).astype(np.int32)
+    tk = np.tile(lst, (Q, 1))[None]
+    cl = np.array([cache.ctx], dtype=np.int32)
+    out, lse = O.sparse_decode_mtp(qn[None], qr[None], cache.pool, cache.stride, cache.block_table, cl, tk, BS,
+                                   0.06, fmt)
+    for i in range(Q):
+        o1, l1 = cache.decode(qn[i], qr[i], lst, 0.06, ctx=cache.ctx - (Q - 1 - i))
+        assert np.array_equal(out[0, i], o1) and np.array_equal(lse[0, i], l1)
+    one, one_lse = O.sparse_decode_mtp(qn[None, :1], qr[None, :1], cache.pool, cache.stride, cache.block_table, cl,
+                                       tk[:, :1], BS, 0.06, fmt)
+    o1, l1 = cache.decode(qn[0], qr[0], lst, 0.06)
+    assert np.array_equal(one[0, 0], o1) and np.array_equal(one_lse[0, 0], l1)
+
+
+def test_draft_tokens_brute_force_softmax(fmt):
+    """Brute force: per token, an explicit softmax over the visible entries of
+    its own list, rows decoded with the OCP tables (not the oracle)."""
+    cache = Cache(130, fmt, seed=33)
+    rng = np.random.default_rng(34)
+    Q, H, k = 4, 2, 20
+    qn = np.stack([rand_q(H, seed=50 + i)[0] for i in range(Q)])
+    qr = np.stack([rand_q(H, seed=50 + i)[1] for i in range(Q)])
+    tk = np.stack([np.concatenate([rng.choice(126, k - 4, replace=False), [126, 127, 128, 129]])
+                   for _ in range(Q)]).astype(np.int32)
+    tk[1, 0] = -1
+    out, lse = O.sparse_decode_mtp(qn[None], qr[None], cache.pool, cache.stride, cache.block_table,
+                                   np.array([130], np.int32), tk[None], BS, 0.08, fmt)
+    for i in range(Q):
+        vis = [t for t in tk[i] if 0 <= t < 130 - (Q - 1 - i)]
+        assert len(vis) == k - (Q - 1 - i) - (1 if i == 1 else 0)
+        rows = [decode_row_indep(cache.row(t), fmt) for t in vis]
+        C_ = np.stack([r[0] for r in rows])
+        R_ = np.stack([r[1] for r in rows])
+        for h in range(H):
+            z = 0.08 * (C_ @ O.bf16_to_f64(qn[i, h]) + R_ @ O.bf16_to_f64(qr[i, h]))
+            p = np.exp(z - z.max())
+            assert lse[0, i, h] == pytest.approx(z.max() + math.log(p.sum()), rel=1e-12, abs=1e-12)
+            assert np.allclose(out[0, i, h], (p / p.sum()) @ C_, rtol=1e-11, atol=1e-12)
