@@ -54,6 +54,7 @@ def parse():
     p.add_argument("--append-sessions", type=int, default=64, help="sessions in the quantize-on-write sub-benchmark")
     p.add_argument("--indexer-batch", type=int, default=64, help="requests in the indexer + top-k sub-benchmark")
     p.add_argument("--only-extras", action="store_true", help="time only the sub-benchmarks (profiling)")
+    p.add_argument("--draft-tokens", type=int, default=4, help="query tokens per request in the draft-token timing")
     return p.parse_args()
 
 
@@ -331,16 +332,31 @@ def main():
                wl.context_lens, wl.topk_idx, wl.softmax_scale, out=wl.out, lse=wl.lse, workspace=ws,
                stream=stream)
 
-    def capture(fmt):
+    # Draft tokens: Q query tokens per request, each with its own top-k list
+    # (90% shared with its neighbours), over the same layer caches.
+    Q = args.draft_tokens
+    drafts = [W.draft_queries(wl, q_len=Q) for wl in layers]
+    ws_mtp = torch.empty(max(m.mla_sparse_decode_mtp_workspace_size(B, Q, H, K), 256), dtype=torch.uint8, device=dev)
+    out_mtp = torch.empty((B, Q, H, 512), dtype=torch.bfloat16, device=dev)
+    lse_mtp = torch.empty((B, Q, H), dtype=torch.float32, device=dev)
+
+    def drafts_all():
+        for wl, dq in zip(layers, drafts):
+            m.mla_sparse_decode_mtp(dq.q_nope, dq.q_rope, wl.pools[0], wl.strides[0], wl.num_blocks, wl.block_table,
+                                    wl.context_lens, dq.topk_idx, wl.softmax_scale, out=out_mtp, lse=lse_mtp,
+                                    workspace=ws_mtp, stream=stream)
+
+    def capture(fn):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
-            decode_all(fmt)  # warm the launch path outside capture
+            fn()  # warm the launch path outside capture
             stream.synchronize()
             with torch.cuda.graph(g, stream=stream):
-                decode_all(fmt)
+                fn()
         return g
 
-    graphs = {0: capture(0), 1: capture(1), 2: capture(2)}
+    graphs = {0: capture(lambda: decode_all(0)), 1: capture(lambda: decode_all(1)), 2: capture(lambda: decode_all(2)),
+              3: capture(drafts_all)}
     torch.cuda.synchronize()
 
     def timed(g, steps, warmup):
@@ -367,6 +383,7 @@ def main():
         ms4 = timed(graphs[0], args.steps, args.warmup)
         ms8 = timed(graphs[1], args.steps, args.warmup)
         ms_st = timed(graphs[2], args.steps, args.warmup)
+        ms_mtp = timed(graphs[3], args.steps, args.warmup)
     clk = clocks.summary()
     splits = m.mla_sparse_decode_workspace_size(B, H, K) > 0
     launches_per_step = L * (2 if splits else 1)
@@ -374,6 +391,9 @@ def main():
     per_layer4 = ms4 / L * 1e-3
     per_layer8 = ms8 / L * 1e-3
     per_layer_st = ms_st / L * 1e-3
+    per_layer_mtp = ms_mtp / L * 1e-3
+    # rows a layer must read at least once: distinct valid entries over a request's Q lists (layer 0)
+    distinct = sum(int(torch.unique(drafts[0].topk_idx[b][drafts[0].topk_idx[b] >= 0]).numel()) for b in range(B))
     rows = B * K
     value = whole_job_rate(rows, world, per_layer4)
     ach4 = layer_bytes4 / per_layer4 / 1e9
@@ -450,6 +470,12 @@ def main():
                    "bytes_per_row": ROW_NVFP4 + 4 + 2 * (ROW_FP8 + 4),
                    "note": "gather kernel writes a 576-byte FP8 copy of each selected row into a buffer every "
                            "layer reuses, then the FP8 decode reads it"},
+        "drafts": {"q_len": Q, "value": whole_job_rate(B * Q * K, world, per_layer_mtp), "unit": UNIT,
+                   "per_layer_us": per_layer_mtp * 1e6, "vs_single_token": per_layer_mtp / per_layer4,
+                   "distinct_rows_per_layer": distinct,
+                   "hbm_gbs_distinct_rows": (distinct * (ROW_NVFP4 + 4) + B * Q * H * 2180) / per_layer_mtp / 1e9,
+                   "note": f"{Q} query tokens per request, each with its own top-2048 list (90% shared), one "
+                           "launch per layer"},
         "nvfp4_bytes_per_row": ROW_NVFP4 + 4,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,

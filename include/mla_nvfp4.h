@@ -215,6 +215,35 @@ mla_status_t mla_sparse_decode_fp8(const uint16_t* q_nope, const uint16_t* q_rop
                                    mla_stream_t stream);
 
 /*
+ * Several query tokens per request, decoded in one launch (speculative draft
+ * tokens: "Prime Inference", section "A kernel that reads four bits
+ * directly" -- the native kernel runs 15 query tokens per launch).  Each
+ * query token has its own top-k list; the q_len tokens of request b are the
+ * last q_len positions of its context_lens[b] tokens, so token i sees only
+ * t < context_lens[b] - (q_len - 1 - i) (entries at or past that bound are
+ * masked like any out-of-context entry).  Otherwise the decode of each token
+ * is exactly that of mla_sparse_decode (fmt MLA_KV_NVFP4) or
+ * mla_sparse_decode_fp8 (fmt MLA_KV_FP8).
+ *
+ *   q_nope        device bf16 [batch, q_len, num_heads, 512]
+ *   q_rope        device bf16 [batch, q_len, num_heads, 64]
+ *   topk_idx      device int32 [batch, q_len, topk]
+ *   q_len         1..64
+ *   out           device bf16 [batch, q_len, num_heads, 512]
+ *   lse           device float [batch, q_len, num_heads], or NULL
+ *   workspace     at least mla_sparse_decode_mtp_workspace_size(batch,
+ *                 q_len, num_heads, topk) bytes, 256-byte aligned
+ * All other arguments as for mla_sparse_decode.
+ */
+size_t mla_sparse_decode_mtp_workspace_size(int batch, int q_len, int num_heads, int topk);
+mla_status_t mla_sparse_decode_mtp(const uint16_t* q_nope, const uint16_t* q_rope, const void* kv_pool,
+                                   int64_t kv_block_stride, int64_t num_blocks, const int32_t* block_table,
+                                   int max_blocks_per_req, const int32_t* context_lens, const int32_t* topk_idx,
+                                   int batch, int q_len, int num_heads, int block_size, int topk, float softmax_scale,
+                                   mla_kv_format_t fmt, uint16_t* out, float* lse, void* workspace,
+                                   size_t workspace_bytes, mla_stream_t stream);
+
+/*
  * Staged path, kept as an ablation of the native decode ("Prime Inference",
  * section "A kernel that reads four bits directly", figure "staged vs native
  * decode": the first version gathered the selected NVFP4 rows, wrote an FP8

@@ -21,7 +21,7 @@ __all__ = [
     "mla_sparse_decode_fp8", "mla_sparse_decode_noalloc", "mla_topk_workspace_size", "mla_topk",
     "mla_indexer_topk_workspace_size", "mla_indexer_topk", "mla_index_key_quantize_append",
     "mla_staged_pool_bytes", "mla_stage_rows_fp8", "mla_sparse_decode_staged_workspace_size",
-    "mla_sparse_decode_staged",
+    "mla_sparse_decode_staged", "mla_sparse_decode_mtp_workspace_size", "mla_sparse_decode_mtp",
 ]
 
 MLA_KV_NVFP4 = 0
@@ -54,6 +54,9 @@ SIGNATURES = {
     "mla_indexer_topk": (_I32, [_P, _P, _P, _I64, _I64, _P, _I32, _P, _I32, _I32, _I32, _I32, _P, _P, _I32, _P,
                                 _SZ, _P]),
     "mla_index_key_quantize_append": (_I32, [_P, _P, _I64, _P, _I64, _I32, _I64, _P]),
+    "mla_sparse_decode_mtp_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
+    "mla_sparse_decode_mtp": (_I32, [_P, _P, _P, _I64, _I64, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _F32,
+                                     _I32, _P, _P, _P, _SZ, _P]),
     "mla_staged_pool_bytes": (_SZ, [_I32, _I32]),
     "mla_stage_rows_fp8": (_I32, [_P, _I64, _I64, _P, _I32, _P, _P, _I32, _I32, _I32, _P, _P, _P]),
     "mla_sparse_decode_staged_workspace_size": (_SZ, [_I32, _I32, _I32]),
@@ -236,6 +239,36 @@ def mla_sparse_decode_staged(q_nope, q_rope, kv_pool, kv_block_stride, num_block
     return _decode("mla_sparse_decode_staged", q_nope, q_rope, kv_pool, kv_block_stride, num_blocks, block_table,
                    context_lens, topk_idx, softmax_scale, block_size, out, lse, workspace, stream,
                    ws_size=mla_sparse_decode_staged_workspace_size)
+
+
+def mla_sparse_decode_mtp_workspace_size(batch: int, q_len: int, num_heads: int, topk: int) -> int:
+    return int(load().mla_sparse_decode_mtp_workspace_size(batch, q_len, num_heads, topk))
+
+
+def mla_sparse_decode_mtp(q_nope, q_rope, kv_pool, kv_block_stride, num_blocks, block_table, context_lens, topk_idx,
+                          softmax_scale, fmt=MLA_KV_NVFP4, block_size=64, out=None, lse=None, workspace=None,
+                          stream=None):
+    """Several query tokens per request: q_nope [B,Q,H,512], q_rope [B,Q,H,64],
+    topk_idx int32 [B,Q,k].  Returns (out bf16 [B,Q,H,512], lse or None)."""
+    q_nope = _bits(q_nope, "q_nope")
+    q_rope = _bits(q_rope, "q_rope")
+    block_table = _contig(block_table, torch.int32, "block_table")
+    context_lens = _contig(context_lens, torch.int32, "context_lens")
+    topk_idx = _contig(topk_idx, torch.int32, "topk_idx")
+    batch, q_len, heads = q_nope.shape[0], q_nope.shape[1], q_nope.shape[2]
+    topk = topk_idx.shape[2]
+    if out is None:
+        out = torch.empty((batch, q_len, heads, 512), dtype=torch.bfloat16, device=q_nope.device)
+    need = mla_sparse_decode_mtp_workspace_size(batch, q_len, heads, topk)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q_nope.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("mla_sparse_decode_mtp",
+           load().mla_sparse_decode_mtp(_ptr(q_nope), _ptr(q_rope), _ptr(kv_pool), kv_block_stride, num_blocks,
+                                        _ptr(block_table), block_table.shape[1], _ptr(context_lens), _ptr(topk_idx),
+                                        batch, q_len, heads, block_size, topk, float(softmax_scale), fmt, _ptr(out),
+                                        _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream)))
+    return out, lse
 
 
 def mla_staged_pool_bytes(batch: int, topk: int) -> int:

@@ -59,23 +59,26 @@ mla_status_t check_decode_args(const uint16_t* q_nope, const uint16_t* q_rope, c
   return MLA_OK;
 }
 
+constexpr int kMaxQueryTokens = 64;
+
 mla_status_t decode_impl(int fmt, const uint16_t* q_nope, const uint16_t* q_rope, const void* kv_pool,
                          int64_t kv_block_stride, int64_t num_blocks, const int32_t* block_table,
                          int max_blocks_per_req, const int32_t* context_lens, const int32_t* topk_idx, int batch,
-                         int num_heads, int block_size, int topk, float softmax_scale, uint16_t* out, float* lse,
-                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                         int q_len, int num_heads, int block_size, int topk, float softmax_scale, uint16_t* out,
+                         float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (q_len < 1 || q_len > kMaxQueryTokens) return MLA_ERR_INVALID_ARG;
   mla_status_t s = check_decode_args(q_nope, q_rope, kv_pool, kv_block_stride, num_blocks, block_table,
                                      max_blocks_per_req, context_lens, topk_idx, batch, num_heads, block_size,
                                      topk, softmax_scale, out, fmt);
   if (s != MLA_OK || batch == 0) return s;
   if (lse && !aligned(lse, 4)) return MLA_ERR_INVALID_ARG;
-  const DecodePlan plan = plan_sparse_decode(batch, num_heads, topk);
+  const DecodePlan plan = plan_sparse_decode(batch * q_len, num_heads, topk);
   if (plan.workspace > 0) {
     if (workspace_bytes < plan.workspace) return MLA_ERR_WORKSPACE_TOO_SMALL;
     if (!workspace || !aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
   }
   return cuda_status(launch_sparse_decode(fmt, q_nope, q_rope, kv_pool, kv_block_stride, num_blocks, block_table,
-                                          max_blocks_per_req, context_lens, topk_idx, batch, num_heads, topk,
+                                          max_blocks_per_req, context_lens, topk_idx, batch, q_len, num_heads, topk,
                                           softmax_scale, out, lse, workspace, plan, stream));
 }
 
@@ -178,8 +181,8 @@ mla_status_t mla_sparse_decode(const uint16_t* q_nope, const uint16_t* q_rope, c
                                uint16_t* out, float* lse, void* workspace, size_t workspace_bytes,
                                mla_stream_t stream) {
   return decode_impl(MLA_KV_NVFP4, q_nope, q_rope, kv_pool, kv_block_stride, num_blocks, block_table,
-                     max_blocks_per_req, context_lens, topk_idx, batch, num_heads, block_size, topk, softmax_scale,
-                     out, lse, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+                     max_blocks_per_req, context_lens, topk_idx, batch, 1, num_heads, block_size, topk,
+                     softmax_scale, out, lse, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 mla_status_t mla_sparse_decode_fp8(const uint16_t* q_nope, const uint16_t* q_rope, const void* kv_pool,
@@ -189,8 +192,8 @@ mla_status_t mla_sparse_decode_fp8(const uint16_t* q_nope, const uint16_t* q_rop
                                    uint16_t* out, float* lse, void* workspace, size_t workspace_bytes,
                                    mla_stream_t stream) {
   return decode_impl(MLA_KV_FP8, q_nope, q_rope, kv_pool, kv_block_stride, num_blocks, block_table,
-                     max_blocks_per_req, context_lens, topk_idx, batch, num_heads, block_size, topk, softmax_scale,
-                     out, lse, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+                     max_blocks_per_req, context_lens, topk_idx, batch, 1, num_heads, block_size, topk,
+                     softmax_scale, out, lse, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 mla_status_t mla_index_key_quantize_append(const uint16_t* keys, const int64_t* slot_mapping, int64_t n_tokens,
@@ -286,8 +289,26 @@ mla_status_t mla_sparse_decode_staged(const uint16_t* q_nope, const uint16_t* q_
   if (e != cudaSuccess) return cuda_status(e);
   const DecodePlan plan = plan_sparse_decode(batch, num_heads, topk);
   return cuda_status(launch_sparse_decode(MLA_KV_FP8, q_nope, q_rope, rows, static_cast<int64_t>(kBlock) * kRowFp8,
-                                          static_cast<int64_t>(batch) * nblk, table, nblk, ctx, list, batch,
+                                          static_cast<int64_t>(batch) * nblk, table, nblk, ctx, list, batch, 1,
                                           num_heads, topk, softmax_scale, out, lse, dec_ws, plan, st));
+}
+
+size_t mla_sparse_decode_mtp_workspace_size(int batch, int q_len, int num_heads, int topk) {
+  if (batch <= 0 || q_len < 1 || q_len > kMaxQueryTokens || num_heads < 16 || num_heads % 16 != 0 || topk < 1)
+    return 0;
+  return plan_sparse_decode(batch * q_len, num_heads, topk).workspace;
+}
+
+mla_status_t mla_sparse_decode_mtp(const uint16_t* q_nope, const uint16_t* q_rope, const void* kv_pool,
+                                   int64_t kv_block_stride, int64_t num_blocks, const int32_t* block_table,
+                                   int max_blocks_per_req, const int32_t* context_lens, const int32_t* topk_idx,
+                                   int batch, int q_len, int num_heads, int block_size, int topk, float softmax_scale,
+                                   mla_kv_format_t fmt, uint16_t* out, float* lse, void* workspace,
+                                   size_t workspace_bytes, mla_stream_t stream) {
+  if (fmt != MLA_KV_NVFP4 && fmt != MLA_KV_FP8) return MLA_ERR_INVALID_ARG;
+  return decode_impl(fmt, q_nope, q_rope, kv_pool, kv_block_stride, num_blocks, block_table, max_blocks_per_req,
+                     context_lens, topk_idx, batch, q_len, num_heads, block_size, topk, softmax_scale, out, lse,
+                     workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t mla_topk_workspace_size(int batch, int max_context_len, int topk) {

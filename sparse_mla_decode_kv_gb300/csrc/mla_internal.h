@@ -27,7 +27,9 @@ cudaError_t launch_stage_rows_fp8(const void* pool, int64_t block_stride, int64_
                                   const int32_t* topk_idx, int batch, int topk, void* staged, int32_t* staged_topk,
                                   int32_t* staged_bt, int32_t* staged_ctx, cudaStream_t stream);
 
-// Sparse decode: split plan and launch.
+// Sparse decode: split plan and launch.  The plan is made for the number of
+// (request, query token) pairs; q_len query tokens per request share its
+// block table and context (token i sees t < ctx - (q_len - 1 - i)).
 struct DecodePlan {
   int splits;          // CTAs per (request, 16-head group) along the top-k list
   int rows_per_split;  // multiple of 16
@@ -37,8 +39,8 @@ DecodePlan plan_sparse_decode(int batch, int num_heads, int topk);
 cudaError_t launch_sparse_decode(int fmt, const uint16_t* q_nope, const uint16_t* q_rope, const void* pool,
                                  int64_t block_stride, int64_t num_blocks, const int32_t* block_table,
                                  int max_blocks_per_req, const int32_t* context_lens, const int32_t* topk_idx,
-                                 int batch, int num_heads, int topk, float softmax_scale, uint16_t* out, float* lse,
-                                 void* workspace, const DecodePlan& plan, cudaStream_t stream);
+                                 int batch, int q_len, int num_heads, int topk, float softmax_scale, uint16_t* out,
+                                 float* lse, void* workspace, const DecodePlan& plan, cudaStream_t stream);
 
 // Indexer and top-k.
 size_t topk_workspace_bytes(int batch, int max_context_len, int topk);

@@ -117,6 +117,7 @@ struct DecodeArgs {
   float* part_lse;  // [B*H, splits], base-2
   int max_blocks;
   int topk;
+  int q_len;  // query tokens per request (1 for plain decode)
   int num_heads;
   int splits;
   int rows_per_split;
@@ -137,14 +138,18 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(const Decode
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int b = blockIdx.x / args.splits;
+  // v = (request, query token) pair: queries, list, output and partials are
+  // indexed by v; the block table and context length by the request b.
+  const int v = blockIdx.x / args.splits;
+  const int b = v / args.q_len;
   const int sp = blockIdx.x % args.splits;
   const int hg = blockIdx.y;
   const int row_begin = sp * args.rows_per_split;
   const int row_end = min(args.topk, row_begin + args.rows_per_split);
   const int n_rows = max(0, row_end - row_begin);
   const int n_stages = (n_rows + kStageRows - 1) / kStageRows;
-  const int ctx = __ldg(args.ctx_lens + b);
+  // query token i of the request's q_len sees t < ctx_b - (q_len - 1 - i)
+  const int ctx = __ldg(args.ctx_lens + b) - (args.q_len - 1 - (v - b * args.q_len));
 
   // The split merge (launched as a programmatic dependent) may start its
   // launch now; it waits for this whole grid before reading any partial.
@@ -161,8 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(const Decode
   // The absorbed query of this warp's dims, loaded first: it does not depend
   // on the row resolution below, so its latency overlaps it.
   const int h0 = hg * kHeadsPerCta + g;
-  const uint16_t* qn0 = args.q_nope + (static_cast<int64_t>(b) * args.num_heads + h0) * kLatent + 128 * w + 8 * c;
-  const uint16_t* qr0 = args.q_rope + (static_cast<int64_t>(b) * args.num_heads + h0) * kRope + 16 * w + 4 * c;
+  const uint16_t* qn0 = args.q_nope + (static_cast<int64_t>(v) * args.num_heads + h0) * kLatent + 128 * w + 8 * c;
+  const uint16_t* qr0 = args.q_rope + (static_cast<int64_t>(v) * args.num_heads + h0) * kRope + 16 * w + 4 * c;
   uint4 qv0[4], qv1[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -175,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(const Decode
   // ---------------------------------------------------------------- rows
   // Resolve every row of the slice (top-k index, then block table) with all
   // threads, in batches of independent loads: two round trips in total.
-  const int32_t* topk_row = args.topk_idx + static_cast<int64_t>(b) * args.topk + row_begin;
+  const int32_t* topk_row = args.topk_idx + static_cast<int64_t>(v) * args.topk + row_begin;
   const int32_t* bt_row = args.block_table + static_cast<int64_t>(b) * args.max_blocks;
   const int n_slots = n_stages * kStageRows;
   for (int base = 0; base < n_slots; base += 4 * kThreads) {
@@ -454,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(const Decode
   const float inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
   const float lse2_0 = l0 > 0.f ? sm.mfin[g] + lg2(l0) : -INFINITY;
   const float lse2_1 = l1 > 0.f ? sm.mfin[g + 8] + lg2(l1) : -INFINITY;
-  const int64_t bh0 = static_cast<int64_t>(b) * args.num_heads + h0;
+  const int64_t bh0 = static_cast<int64_t>(v) * args.num_heads + h0;
   const int64_t bh1 = bh0 + 8;
 
   if (args.splits == 1) {
@@ -580,9 +585,10 @@ DecodePlan plan_sparse_decode(int batch, int num_heads, int topk) {
 cudaError_t launch_sparse_decode(int fmt, const uint16_t* q_nope, const uint16_t* q_rope, const void* pool,
                                  int64_t block_stride, int64_t num_blocks, const int32_t* block_table,
                                  int max_blocks_per_req, const int32_t* context_lens, const int32_t* topk_idx,
-                                 int batch, int num_heads, int topk, float softmax_scale, uint16_t* out, float* lse,
-                                 void* workspace, const DecodePlan& plan, cudaStream_t stream) {
-  if (batch <= 0) return cudaSuccess;
+                                 int batch, int q_len, int num_heads, int topk, float softmax_scale, uint16_t* out,
+                                 float* lse, void* workspace, const DecodePlan& plan, cudaStream_t stream) {
+  const int pairs = batch * q_len;  // (request, query token) pairs
+  if (pairs <= 0) return cudaSuccess;
   DecodeArgs a;
   a.q_nope = q_nope;
   a.q_rope = q_rope;
@@ -596,6 +602,7 @@ cudaError_t launch_sparse_decode(int fmt, const uint16_t* q_nope, const uint16_t
   a.lse = lse;
   a.max_blocks = max_blocks_per_req;
   a.topk = topk;
+  a.q_len = q_len;
   a.num_heads = num_heads;
   a.splits = plan.splits;
   a.rows_per_split = plan.rows_per_split;
@@ -605,15 +612,15 @@ cudaError_t launch_sparse_decode(int fmt, const uint16_t* q_nope, const uint16_t
   a.fault_word = fault_word_ptr();
   if (a.fault_word == nullptr) return cudaErrorInvalidDevicePointer;
   if (plan.splits > 1) {
-    const size_t n_bh = static_cast<size_t>(batch) * num_heads;
+    const size_t n_bh = static_cast<size_t>(pairs) * num_heads;
     size_t o_bytes = n_bh * plan.splits * kLatent * sizeof(float);
     o_bytes = (o_bytes + 255) / 256 * 256;
     a.part_o = static_cast<float*>(workspace);
     a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + o_bytes);
   }
-  cudaError_t e = fmt == 0 ? launch_fmt<0>(a, batch, stream) : launch_fmt<1>(a, batch, stream);
+  cudaError_t e = fmt == 0 ? launch_fmt<0>(a, pairs, stream) : launch_fmt<1>(a, pairs, stream);
   if (e != cudaSuccess || plan.splits == 1) return e;
-  const int64_t n_bh = static_cast<int64_t>(batch) * num_heads;
+  const int64_t n_bh = static_cast<int64_t>(pairs) * num_heads;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(n_bh));
   cfg.blockDim = dim3(128);

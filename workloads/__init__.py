@@ -166,6 +166,46 @@ def tp4_rank_decode(device, seed: int = 0, batch: int = 32, ctx: int = 140_000, 
                             draw)
 
 
+@dataclass
+class DraftQueries:
+    """q_len query tokens per request of a decode workload: queries and one
+    top-k list per token."""
+    q_len: int
+    q_nope: torch.Tensor     # bf16 [B,Q,H,512]
+    q_rope: torch.Tensor     # bf16 [B,Q,H,64]
+    topk_idx: torch.Tensor   # int32 [B,Q,k]
+
+
+def draft_queries(wl: DecodeWorkload, q_len: int = 4, keep: float = 0.9, recent: int = 6000,
+                  seed: int = 0) -> DraftQueries:
+    """Speculative draft tokens for the requests of `wl` (its context lengths
+    count the q_len new tokens).  Token i's list keeps a random `keep`
+    fraction of the request's list in `wl` and fills the rest with distinct
+    positions from the last `recent` tokens (lists of neighbouring tokens
+    overlap, as an indexer's would); ascending."""
+    dev = wl.q_nope.device
+    B, H, k = wl.batch, wl.heads, wl.topk
+    gq = generator(dev, *wl.seed_parts, "draft", seed, "q")
+    qn = bf16_normal((B, q_len, H, LATENT), gq, dev)
+    qr = bf16_normal((B, q_len, H, ROPE), gq, dev)
+    idx = torch.full((B, q_len, k), -1, dtype=torch.int32, device=dev)
+    for b in range(B):
+        base = wl.topk_idx[b]
+        base = base[base >= 0].to(torch.int64)
+        n = base.numel()
+        c = int(wl.context_lens[b])
+        for i in range(q_len):
+            g = generator(dev, *wl.seed_parts, "draft", seed, "topk", b, i)
+            n_keep = int(round(keep * n))
+            kept = base[torch.randperm(n, generator=g, device=dev)[:n_keep]]
+            lo = max(0, c - recent)
+            cand = distinct_uniform(min(c - lo, 3 * (n - n_keep) + 64), lo, c, g, dev).to(torch.int64)
+            cand = cand[~torch.isin(cand, kept)][:n - n_keep]
+            sel = torch.sort(torch.cat([kept, cand])).values.to(torch.int32)
+            idx[b, i, :sel.numel()] = sel
+    return DraftQueries(q_len, qn, qr, idx)
+
+
 def dep_rank_context_lens(seed: int = 0, batch: int = 128, lo: int = 8192, hi: int = 1 << 20,
                           cap: int = 24_000_000) -> List[int]:
     """Context lengths log-uniform in [lo, hi]; if they sum past `cap` they are
