@@ -128,15 +128,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait for the phase with the given parity.  try_wait itself parks
-// the thread for a hardware-chosen interval, so the first polls spin; only
-// after kSpinPolls does the loop back off with nanosleep.  Returns false
-// (after setting `fault` in *fault_word) if the phase never completed.
+// try_wait with a suspend-time hint: the thread may sleep in hardware (up to
+// `hint_ns`) until the phase completes instead of spinning on issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3; "
+      "selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase with the given parity.  The first kSpinPolls
+// tries sleep in hardware between polls (woken when the phase completes);
+// after them the loop backs off with nanosleep.  Returns false (after
+// setting `fault` in *fault_word) if the phase never completed.
 constexpr uint32_t kSpinPolls = 1u << 14;
+constexpr uint32_t kSleepHintNs = 20000;
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned int* fault_word,
                                                   unsigned int fault) {
   for (uint32_t i = 0; i < kSpinPolls; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
   uint32_t ns = 64;
   for (uint32_t i = 0; i < kWaitPolls; ++i) {
     __nanosleep(ns);

@@ -46,8 +46,12 @@
 //    merge kernel, launched as a programmatic dependent of the decode grid,
 //    combines them (the pages merge in-cluster through distributed shared
 //    memory; this build uses a second launch).
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+
+#include <cstring>
+#include <mutex>
 
 #include "mla_device.cuh"
 #include "mla_internal.h"
@@ -59,7 +63,7 @@ constexpr int kConsumerWarps = 4;
 constexpr int kThreads = kConsumerWarps * 32;  // all warps consume; warp 0 also refills stages
 constexpr int kStageRows = 32;  // one stage = one phase = two 16-row m-tiles
 constexpr int kHeadsPerCta = 16;
-constexpr int kMaxRows = 2048;  // rows of one CTA's slice (top-k <= 2048)
+constexpr int kMaxRows = 1024;  // list entries of one CTA's slice (the plan never exceeds it)
 constexpr int kRedPitch = 24;  // floats per token row of the partial-score exchange
 constexpr int kPPitch = 40;    // halfs per head row of P (80 bytes: ldmatrix conflict-free)
 constexpr int kKSteps = 9;     // k-steps of 16 dims per consumer warp (128 latent + 16 rope)
@@ -86,9 +90,15 @@ struct Fmt<1> {
   static constexpr int kStages = 3;  // two CTAs per SM still fit
 };
 
-template <int FMT>
+// Row pitch in the shared-memory ring: the 16-byte pad that makes the
+// fragment loads conflict-free is only possible with per-chunk copies; a
+// 4-row TMA gather writes its rows back to back.
+template <int FMT, bool TMA>
+constexpr int row_pitch() { return TMA ? Fmt<FMT>::kRowBytes : Fmt<FMT>::kPitch; }
+
+template <int FMT, bool TMA>
 struct alignas(128) Smem {
-  uint8_t rows[Fmt<FMT>::kStages][kStageRows][Fmt<FMT>::kPitch];
+  uint8_t rows[Fmt<FMT>::kStages][kStageRows][row_pitch<FMT, TMA>()];
   uint4 qfrag[kConsumerWarps][kKSteps][32];  // query B fragments, fragment order
   float red[kConsumerWarps][kStageRows][kRedPitch];
   __half pbuf[kHeadsPerCta][kPPitch];
@@ -96,7 +106,7 @@ struct alignas(128) Smem {
   int rescale[kConsumerWarps];
   float mfin[kHeadsPerCta];
   float lfin[kHeadsPerCta];
-  int64_t row_off[kMaxRows];  // byte offset of each row of the slice in the pool
+  int64_t row_off[kMaxRows];  // per row of the slice: byte offset in the pool (TMA: row index), -1 if masked
   int32_t tok_all[kMaxRows];  // token of each row of the slice, -1 if masked
   uint64_t full[Fmt<FMT>::kStages];
   int abort_flag;
@@ -129,12 +139,34 @@ __device__ __forceinline__ uint32_t bf16pair_to_f16x2(uint32_t two) {
   return f32x2_to_f16x2_sat(bf16_bits_to_f32(two & 0xFFFFu), bf16_bits_to_f32(two >> 16));
 }
 
-template <int FMT>
-__global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(const DecodeArgs args) {
+// 4-row TMA gather: rows y0..y3 of the pool viewed as a 2-D tensor
+// [rows][row bytes / 8] (8-byte elements), one row high per box; a negative
+// row index reads zeros.  Completion is signalled on `bar` as transaction
+// bytes.
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* tmap, int y0, int y1, int y2, int y3,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(0), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+// TMA = true: rows are gathered by TMA, 4 rows per instruction (the pool's
+// block stride is a whole number of rows, so the pool is a 2-D tensor of
+// rows); false: every thread copies 16-byte chunks with cp.async.
+template <int FMT, bool TMA>
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_decode_kernel(const DecodeArgs args, const __grid_constant__ CUtensorMap tmap) {
   using F = Fmt<FMT>;
   constexpr int kStages = F::kStages;
+  constexpr int kPitchB = row_pitch<FMT, TMA>();
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  Smem<FMT>& sm = *reinterpret_cast<Smem<FMT>*>(smem_raw);
+  Smem<FMT, TMA>& sm = *reinterpret_cast<Smem<FMT, TMA>*>(smem_raw);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -151,11 +183,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(const Decode
   // query token i of the request's q_len sees t < ctx_b - (q_len - 1 - i)
   const int ctx = __ldg(args.ctx_lens + b) - (args.q_len - 1 - (v - b * args.q_len));
 
+  // This grid is launched as a programmatic dependent of whatever precedes it
+  // on the stream: its CTAs may be resident early, but nothing is read before
+  // the preceding grid has completed and its writes are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // The split merge (launched as a programmatic dependent) may start its
   // launch now; it waits for this whole grid before reading any partial.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&sm.full[s], kThreads);
+    for (int s = 0; s < kStages; ++s) mbar_init(&sm.full[s], TMA ? kConsumerWarps : kThreads);
     sm.abort_flag = 0;
     fence_mbar_init();
   }
@@ -202,26 +238,45 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(const Decode
       const bool ok = pb[u] >= 0 && pb[u] < args.num_blocks;
       if (j < n_slots) {
         sm.tok_all[j] = ok ? t[u] : -1;
-        sm.row_off[j] = ok ? static_cast<int64_t>(pb[u]) * args.block_stride +
-                                 static_cast<int64_t>(t[u] % kBlock) * F::kRowBytes
-                           : -1;
+        if constexpr (TMA)
+          sm.row_off[j] = ok ? static_cast<int64_t>(pb[u]) * (args.block_stride / F::kRowBytes) + t[u] % kBlock : -1;
+        else
+          sm.row_off[j] = ok ? static_cast<int64_t>(pb[u]) * args.block_stride +
+                                   static_cast<int64_t>(t[u] % kBlock) * F::kRowBytes
+                             : -1;
       }
     }
   }
   __syncthreads();  // barrier init and the resolved rows are visible
 
-  // All threads fill stage `it` into its ring slot with 16-byte cp.async
-  // (masked rows zero-filled), then arrive on full[slot] when theirs land.
+  // Fill stage `it` into its ring slot; masked rows arrive as zeros.
+  // TMA: lane 0 of every warp posts its share of the stage's bytes on
+  // full[slot] and issues two 4-row gathers (rows 8w .. 8w+7).  cp.async:
+  // every thread copies its 16-byte chunks, then arrives on full[slot] when
+  // they land.
   constexpr int kChunks = F::kRowBytes / 16;
   auto fill_stage = [&](int it) {
     const int slot = it % kStages;
-    for (int i = threadIdx.x; i < kStageRows * kChunks; i += kThreads) {
-      const int r = i / kChunks, k = i - (i / kChunks) * kChunks;
-      const int64_t off = sm.row_off[it * kStageRows + r];
-      const uint8_t* src = args.pool + (off >= 0 ? off : 0) + 16 * k;
-      cp_async16(sm.rows[slot][r] + 16 * k, src, off >= 0 ? 16u : 0u);
+    if constexpr (TMA) {
+      if (lane == 0) {
+        constexpr int kWarpRows = kStageRows / kConsumerWarps;  // 8
+        mbar_expect_tx(&sm.full[slot], kWarpRows * F::kRowBytes);
+        const int64_t* y = sm.row_off + it * kStageRows + kWarpRows * warp;
+#pragma unroll
+        for (int k = 0; k < kWarpRows / 4; ++k)
+          tma_gather4(sm.rows[slot][kWarpRows * warp + 4 * k], &tmap, static_cast<int>(y[4 * k]),
+                      static_cast<int>(y[4 * k + 1]), static_cast<int>(y[4 * k + 2]), static_cast<int>(y[4 * k + 3]),
+                      &sm.full[slot]);
+      }
+    } else {
+      for (int i = threadIdx.x; i < kStageRows * kChunks; i += kThreads) {
+        const int r = i / kChunks, k = i - (i / kChunks) * kChunks;
+        const int64_t off = sm.row_off[it * kStageRows + r];
+        const uint8_t* src = args.pool + (off >= 0 ? off : 0) + 16 * k;
+        cp_async16(sm.rows[slot][r] + 16 * k, src, off >= 0 ? 16u : 0u);
+      }
+      cp_async_arrive(&sm.full[slot]);
     }
-    cp_async_arrive(&sm.full[slot]);
   };
   // Only two stages up front: the copies of every CTA start together, and a
   // deeper initial burst would only delay the first stage behind the others.
@@ -262,6 +317,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(const Decode
   for (int it = 0; it < n_stages && !aborted; ++it) {
     const int slot = it % kStages;
     const uint32_t round = it / kStages;
+    if constexpr (TMA) {
+      // Every warp finished reading stage it - 1's slot before the first
+      // barrier of that stage, so stages up to it - 1 + kStages may be issued.
+      for (; next_fill < n_stages && next_fill <= it - 1 + kStages; ++next_fill) fill_stage(next_fill);
+    }
     const bool ok = mbar_wait_bounded(&sm.full[slot], round & 1u, args.fault_word, kFaultDecodeWait);
     if (!__all_sync(0xFFFFFFFFu, ok) && lane == 0) sm.abort_flag = 1;  // all warps leave after the next barrier
     const uint8_t* base = sm.rows[slot][0];
@@ -270,8 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(const Decode
     uint32_t a[2][kKSteps][4];
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt) {
-      const uint8_t* row0 = base + (16 * mt + g) * F::kPitch;
-      const uint8_t* row1 = row0 + 8 * F::kPitch;
+      const uint8_t* row0 = base + (16 * mt + g) * kPitchB;
+      const uint8_t* row1 = row0 + 8 * kPitchB;
       if constexpr (FMT == 0) {
         // Scales of groups 8w + 2q + (c>>1), q = 0..3: one 8-byte load per row,
         // a byte permute and a conversion per pair, then {S, S} duplicates.
@@ -354,7 +414,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(const Decode
     }
     // Every warp has finished reading the rows of stages <= it, so stages up
     // to it + kStages may be issued; at most two per boundary.
-    for (int k = 0; k < 2 && next_fill < n_stages && next_fill <= it + kStages; ++k) fill_stage(next_fill++);
+    if constexpr (!TMA)
+      for (int k = 0; k < 2 && next_fill < n_stages && next_fill <= it + kStages; ++k) fill_stage(next_fill++);
 
     // ---- head owner: heads 4w..4w+3 of token `lane`
     {
@@ -512,8 +573,10 @@ __global__ void __launch_bounds__(128) splitk_merge_kernel(const float* __restri
                                                            const float* __restrict__ part_lse, int splits,
                                                            uint16_t* __restrict__ out, float* __restrict__ lse) {
   // Launched as a programmatic dependent of the decode: wait until that grid
-  // has completed and its partials are visible.
+  // has completed and its partials are visible.  What follows on the stream
+  // may launch early (it waits for this grid the same way).
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t bh = blockIdx.x;
   const int t = threadIdx.x;
   const float* pl = part_lse + bh * splits;
@@ -541,22 +604,78 @@ __global__ void __launch_bounds__(128) splitk_merge_kernel(const float* __restri
   if (lse != nullptr && t == 0) lse[bh] = wsum > 0.f ? (mx + lg2(wsum)) * kLn2 : -INFINITY;
 }
 
-template <int FMT>
-cudaError_t launch_fmt(const DecodeArgs& a, int batch, cudaStream_t stream) {
-  const size_t smem = sizeof(Smem<FMT>);
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library); null if unavailable.
+EncodeTiledFn encode_tiled() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// The pool as a 2-D tensor of rows for the 4-row gather: [rows][row bytes / 8]
+// with 8-byte elements, rows row_bytes apart (the block stride is a whole
+// number of rows), box one row high.  False if the pool cannot be described.
+bool make_row_tensor_map(CUtensorMap* map, const void* pool, int64_t block_stride, int64_t num_blocks, int row_bytes) {
+  if (block_stride % row_bytes != 0 || num_blocks <= 0) return false;
+  const int64_t rows = num_blocks * (block_stride / row_bytes);
+  if (rows > 0x7FFFFFFF) return false;  // row coordinates are 32-bit
+  EncodeTiledFn fn = encode_tiled();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes / 8), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(row_bytes / 8), 1u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(pool), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int FMT, bool TMA>
+cudaError_t launch_variant(const DecodeArgs& a, const CUtensorMap& map, int pairs, cudaStream_t stream) {
+  const size_t smem = sizeof(Smem<FMT, TMA>);
   static int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(sparse_decode_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(sparse_decode_kernel<FMT, TMA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  dim3 grid(batch * a.splits, a.num_heads / kHeadsPerCta);
-  sparse_decode_kernel<FMT><<<grid, kThreads, smem, stream>>>(a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pairs * a.splits, a.num_heads / kHeadsPerCta);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, sparse_decode_kernel<FMT, TMA>, a, map);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+template <int FMT>
+cudaError_t launch_fmt(const DecodeArgs& a, int pairs, cudaStream_t stream) {
+  CUtensorMap map;
+  if (make_row_tensor_map(&map, a.pool, a.block_stride, a.num_blocks, Fmt<FMT>::kRowBytes))
+    return launch_variant<FMT, true>(a, map, pairs, stream);
+  memset(&map, 0, sizeof(map));
+  return launch_variant<FMT, false>(a, map, pairs, stream);
 }
 
 }  // namespace
@@ -567,7 +686,8 @@ DecodePlan plan_sparse_decode(int batch, int num_heads, int topk) {
   const int slots = 2 * device_sm_count();  // two CTAs per SM fit (registers, shared memory)
   int splits = groups > 0 ? slots / groups : 1;
   const int max_splits = (topk + kStageRows - 1) / kStageRows;
-  splits = splits < 1 ? 1 : (splits > max_splits ? max_splits : splits);
+  const int min_splits = (topk + kMaxRows - 1) / kMaxRows;  // a slice fits the CTA's row tables
+  splits = splits < min_splits ? min_splits : (splits > max_splits ? max_splits : splits);
   int rows = (topk + splits - 1) / splits;
   rows = (rows + 15) / 16 * 16;
   splits = (topk + rows - 1) / rows;
