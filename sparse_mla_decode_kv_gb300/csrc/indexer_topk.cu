@@ -167,6 +167,138 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 3) indexer_scores_kernel(const
   }
 }
 
+// TMA variant (the pool's block stride is a multiple of 128 bytes, so the key
+// pool is a 2-D tensor of 128-byte rows): the CTA's 8 key blocks (64 tokens
+// x 128 bytes each) land in shared memory as 8 tiles with the 128-byte
+// swizzle, their scales as 8 bulk copies of 256 bytes, all issued at entry
+// (66 KB in flight per CTA); each block has its own mbarrier so the warps
+// start on block 0 while the rest arrive.  The swizzle puts the 16-byte
+// chunk j of tile row r at chunk j ^ (r & 7), so the 8 rows a fragment load
+// touches hit 8 different bank groups.
+constexpr int kIdxBlocksPerCta = kIdxTokensPerCta / kBlock;  // 8
+
+struct alignas(1024) IdxSmem {
+  uint8_t keys[kIdxBlocksPerCta][kBlock][kIdxDim];  // 8 KB per block, 1024-byte aligned (swizzle atom)
+  float scales[kIdxBlocksPerCta][kBlock];
+  uint64_t bar[kIdxBlocksPerCta];
+  int32_t pblk[kIdxBlocksPerCta];  // physical block, -1 if invalid or past the context
+};
+
+template <int NT>  // n-tiles of 8 heads
+__global__ void __launch_bounds__(kIdxWarps * 32, 3)
+    indexer_scores_tma_kernel(const IdxArgs a, const __grid_constant__ CUtensorMap tmap, unsigned int* fault_word) {
+  extern __shared__ uint8_t idx_smem_raw[];
+  // The swizzled tiles need a 1024-byte aligned base.
+  IdxSmem& sm = *reinterpret_cast<IdxSmem*>(idx_smem_raw + ((1024u - (smem_u32(idx_smem_raw) & 1023u)) & 1023u));
+  const int b = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int ctx = min(__ldg(a.ctx_lens + b), a.max_ctx);
+  const int t_begin = blockIdx.x * kIdxTokensPerCta;
+  if (t_begin >= ctx) return;
+  const int32_t* bt_row = a.block_table + static_cast<int64_t>(b) * a.max_blocks;
+  const int lb0 = t_begin / kBlock;
+
+  if (threadIdx.x < kIdxBlocksPerCta) {
+    const int lb = lb0 + threadIdx.x;
+    int pb = -1;
+    if (lb * kBlock < ctx && lb < a.max_blocks) {
+      pb = __ldg(bt_row + lb);
+      if (pb < 0 || pb >= a.num_blocks) pb = -1;
+    }
+    sm.pblk[threadIdx.x] = pb;
+    mbar_init(&sm.bar[threadIdx.x], 1);
+  }
+  fence_mbar_init();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int64_t rows_per_block = a.block_stride / kIdxDim;
+#pragma unroll 1
+    for (int i = 0; i < kIdxBlocksPerCta; ++i) {
+      const int pb = sm.pblk[i];
+      if (pb < 0) continue;
+      mbar_expect_tx(&sm.bar[i], kIdxBlockBytesKeys + kBlock * 4);
+      tma_load_2d(sm.keys[i][0], &tmap, 0, static_cast<int>(pb * rows_per_block), &sm.bar[i]);
+      bulk_load(sm.scales[i], a.pool + static_cast<int64_t>(pb) * a.block_stride + kIdxBlockBytesKeys, kBlock * 4,
+                &sm.bar[i]);
+    }
+  }
+
+  // Query B fragments (K = 128 dims permuted like the keys, N = 8*NT heads) and head weights.
+  uint32_t bq[8][NT][2];
+  float wh[NT][2];
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+    const int h = 8 * n + g;
+    const uint16_t* qh = a.q + (static_cast<int64_t>(b) * a.n_heads + h) * kIdxDim;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(qh + 32 * q + 8 * c));
+      bq[2 * q][n][0] = bf16pair_to_f16x2(v.x);
+      bq[2 * q][n][1] = bf16pair_to_f16x2(v.y);
+      bq[2 * q + 1][n][0] = bf16pair_to_f16x2(v.z);
+      bq[2 * q + 1][n][1] = bf16pair_to_f16x2(v.w);
+    }
+    const float* wb = a.w + static_cast<int64_t>(b) * a.n_heads;
+    wh[n][0] = __ldg(wb + 8 * n + 2 * c);
+    wh[n][1] = __ldg(wb + 8 * n + 2 * c + 1);
+  }
+
+  float* out_row = a.scores + static_cast<int64_t>(b) * a.scores_stride;
+  constexpr int kTiles = kIdxTokensPerCta / 16;
+  for (int mt = warp; mt < kTiles && t_begin + 16 * mt < ctx; mt += kIdxWarps) {
+    const int blk = mt / (kBlock / 16);
+    const int r0 = (mt % (kBlock / 16)) * 16 + g;  // tile rows r0 and r0 + 8; (r & 7) == g for both
+    const int t0 = t_begin + 16 * mt + g;
+    const int t1 = t0 + 8;
+    if (sm.pblk[blk] < 0) {  // block id outside the pool: the block's tokens score -inf
+      if (c == 0) {
+        if (t0 < ctx) out_row[t0] = -INFINITY;
+        if (t1 < ctx) out_row[t1] = -INFINITY;
+      }
+      continue;
+    }
+    if (!mbar_wait_bounded(&sm.bar[blk], 0u, fault_word, kFaultIndexerWait)) continue;
+    const uint8_t* row0 = sm.keys[blk][r0];
+    const uint8_t* row1 = sm.keys[blk][r0 + 8];
+    float acc[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int off = (((2 * q + (c >> 1)) ^ g) << 4) + 8 * (c & 1);
+      const uint2 v0 = *reinterpret_cast<const uint2*>(row0 + off);
+      const uint2 v1 = *reinterpret_cast<const uint2*>(row1 + off);
+      uint32_t A0[4] = {e4m3x2_to_f16x2(v0.x), e4m3x2_to_f16x2(v1.x), e4m3x2_to_f16x2(v0.x >> 16),
+                        e4m3x2_to_f16x2(v1.x >> 16)};
+      uint32_t A1[4] = {e4m3x2_to_f16x2(v0.y), e4m3x2_to_f16x2(v1.y), e4m3x2_to_f16x2(v0.y >> 16),
+                        e4m3x2_to_f16x2(v1.y >> 16)};
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        mma_f16(acc[n], A0, bq[2 * q][n][0], bq[2 * q][n][1]);
+        mma_f16(acc[n], A1, bq[2 * q + 1][n][0], bq[2 * q + 1][n][1]);
+      }
+    }
+    const float s0 = sm.scales[blk][r0];
+    const float s1 = sm.scales[blk][r0 + 8];
+    // sum_h w_h * relu(s_t * dot): this lane holds heads 8n + 2c + {0,1}.
+    float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      p0 += wh[n][0] * fmaxf(s0 * acc[n][0], 0.f) + wh[n][1] * fmaxf(s0 * acc[n][1], 0.f);
+      p1 += wh[n][0] * fmaxf(s1 * acc[n][2], 0.f) + wh[n][1] * fmaxf(s1 * acc[n][3], 0.f);
+    }
+    p0 += __shfl_xor_sync(0xFFFFFFFFu, p0, 1);
+    p0 += __shfl_xor_sync(0xFFFFFFFFu, p0, 2);
+    p1 += __shfl_xor_sync(0xFFFFFFFFu, p1, 1);
+    p1 += __shfl_xor_sync(0xFFFFFFFFu, p1, 2);
+    if (c == 0) {
+      if (t0 < ctx) out_row[t0] = p0;
+      if (t1 < ctx) out_row[t1] = p1;
+    }
+  }
+}
+
 // ----------------------------------------------------------------- top-k
 constexpr int kTopkThreads = 1024;
 constexpr int kHistBins = 2048;
@@ -470,6 +602,23 @@ cudaError_t launch_topk(const float* scores, int64_t row_stride, const int32_t* 
   return cudaGetLastError();
 }
 
+template <int NT>
+cudaError_t launch_idx_tma(const IdxArgs& a, const CUtensorMap& map, unsigned int* fw, dim3 grid, size_t smem,
+                           cudaStream_t stream) {
+  static int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(indexer_scores_tma_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  indexer_scores_tma_kernel<NT><<<grid, kIdxWarps * 32, smem, stream>>>(a, map, fw);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_indexer_scores(const uint16_t* q_idx, const float* head_w, const void* key_pool,
                                   int64_t block_stride, int64_t num_blocks, const int32_t* block_table,
                                   int max_blocks_per_req, const int32_t* context_lens, int batch, int n_heads,
@@ -489,6 +638,21 @@ cudaError_t launch_indexer_scores(const uint16_t* q_idx, const float* head_w, co
   a.n_heads = n_heads;
   a.max_ctx = max_context_len;
   dim3 grid((max_context_len + kIdxTokensPerCta - 1) / kIdxTokensPerCta, batch);
+  CUtensorMap map;
+  const int64_t rows = num_blocks * (block_stride / kIdxDim);
+  unsigned int* fw = fault_word_ptr();
+  if (fw != nullptr && num_blocks > 0 && block_stride % kIdxDim == 0 && rows <= 0x7FFFFFFF &&
+      encode_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, key_pool, kIdxDim, rows, kIdxDim, kIdxDim, kBlock,
+                           CU_TENSOR_MAP_SWIZZLE_128B)) {
+    const size_t smem = sizeof(IdxSmem) + 1024;
+    switch (n_heads / 8) {
+      case 1: return launch_idx_tma<1>(a, map, fw, grid, smem, stream);
+      case 2: return launch_idx_tma<2>(a, map, fw, grid, smem, stream);
+      case 4: return launch_idx_tma<4>(a, map, fw, grid, smem, stream);
+      case 8: return launch_idx_tma<8>(a, map, fw, grid, smem, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (n_heads / 8) {
     case 1: indexer_scores_kernel<1><<<grid, kIdxWarps * 32, 0, stream>>>(a); break;
     case 2: indexer_scores_kernel<2><<<grid, kIdxWarps * 32, 0, stream>>>(a); break;

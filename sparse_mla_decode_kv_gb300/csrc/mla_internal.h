@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace mla {
@@ -12,6 +13,13 @@ namespace mla {
 int device_sm_count();
 // Device address of the library's fault word on the current device.
 unsigned int* fault_word_ptr();
+// A 2-D TMA tensor map (no interleave, zero fill out of bounds) over `rows`
+// rows of `inner` elements, rows `row_stride` bytes apart; box
+// {box_inner, box_rows}.  False when the driver entry point is unavailable
+// or the description is rejected.
+bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, uint64_t inner,
+                          uint64_t rows, uint64_t row_stride, uint32_t box_inner, uint32_t box_rows,
+                          CUtensorMapSwizzle swizzle);
 
 cudaError_t launch_quantize_append(const uint16_t* latent, const uint16_t* rope, const int64_t* slot_mapping,
                                    int64_t n_tokens, void* pool, int64_t num_blocks, int64_t block_stride, int fmt,

@@ -51,7 +51,6 @@
 #include <cuda_fp16.h>
 
 #include <cstring>
-#include <mutex>
 
 #include "mla_device.cuh"
 #include "mla_internal.h"
@@ -137,23 +136,6 @@ struct DecodeArgs {
 
 __device__ __forceinline__ uint32_t bf16pair_to_f16x2(uint32_t two) {
   return f32x2_to_f16x2_sat(bf16_bits_to_f32(two & 0xFFFFu), bf16_bits_to_f32(two >> 16));
-}
-
-// 4-row TMA gather: rows y0..y3 of the pool viewed as a 2-D tensor
-// [rows][row bytes / 8] (8-byte elements), one row high per box; a negative
-// row index reads zeros.  Completion is signalled on `bar` as transaction
-// bytes.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* tmap, int y0, int y1, int y2, int y3,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(0), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
-      : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
 }
 
 // TMA = true: rows are gathered by TMA, 4 rows per instruction (the pool's
@@ -604,25 +586,6 @@ __global__ void __launch_bounds__(128) splitk_merge_kernel(const float* __restri
   if (lse != nullptr && t == 0) lse[bh] = wsum > 0.f ? (mx + lg2(wsum)) * kLn2 : -INFINITY;
 }
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
-// against the driver library); null if unavailable.
-EncodeTiledFn encode_tiled() {
-  static std::once_flag once;
-  static EncodeTiledFn fn = nullptr;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
-
 // The pool as a 2-D tensor of rows for the 4-row gather: [rows][row bytes / 8]
 // with 8-byte elements, rows row_bytes apart (the block stride is a whole
 // number of rows), box one row high.  False if the pool cannot be described.
@@ -630,15 +593,8 @@ bool make_row_tensor_map(CUtensorMap* map, const void* pool, int64_t block_strid
   if (block_stride % row_bytes != 0 || num_blocks <= 0) return false;
   const int64_t rows = num_blocks * (block_stride / row_bytes);
   if (rows > 0x7FFFFFFF) return false;  // row coordinates are 32-bit
-  EncodeTiledFn fn = encode_tiled();
-  if (fn == nullptr) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes / 8), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(row_bytes / 8), 1u};
-  const cuuint32_t estr[2] = {1u, 1u};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(pool), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_tensor_map_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, pool, row_bytes / 8, rows, row_bytes,
+                              row_bytes / 8, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 template <int FMT, bool TMA>
