@@ -22,59 +22,88 @@ namespace {
 
 constexpr int kWarpsPerBlock = 8;
 
+// x / d (d > 0) rounded to nearest-even, i.e. the IEEE float32 quotient,
+// from the correctly rounded reciprocal and one FMA correction step
+// (Markstein's theorem: with r = RN(1/d) and q0 = RN(x r),
+// RN(q0 + RN(x - q0 d) r) = RN(x/d) while quotient and residual stay in the
+// normal range).  Tiny quotients (x subnormal) round to 0 in both e2m1 and
+// e4m3 whichever way their last bit goes.  The correction turns -0 into +0,
+// so the quotient takes x's sign explicitly.
+__device__ __forceinline__ float div_rn(float x, float d, float r) {
+  const float q0 = __fmul_rn(x, r);
+  const float e = __fmaf_rn(-q0, d, x);
+  return copysignf(__fmaf_rn(e, r, q0), x);
+}
+
 template <int FMT>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     quantize_append_kernel(const uint16_t* __restrict__ latent, const uint16_t* __restrict__ rope,
                            const int64_t* __restrict__ slot_mapping, int64_t n_tokens, uint8_t* __restrict__ pool,
                            int64_t num_blocks, int64_t block_stride) {
+  constexpr int kUnroll = 2;  // tokens per warp per iteration: all their loads are issued first
   const int lane = threadIdx.x & 31;
   const int64_t warp_global = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
   const int64_t warp_stride = static_cast<int64_t>(gridDim.x) * kWarpsPerBlock;
-  for (int64_t n = warp_global; n < n_tokens; n += warp_stride) {
-    const int64_t slot = __ldg(slot_mapping + n);
-    if (slot < 0 || slot / kBlock >= num_blocks) continue;  // skipped (warp-uniform)
-    uint8_t* row = pool + (slot / kBlock) * block_stride + (slot % kBlock) * (FMT == 0 ? kRowNvfp4 : kRowFp8);
-
-    // 16 latent values of group `lane`, as two 16-byte loads.
-    const uint4* src = reinterpret_cast<const uint4*>(latent + n * kLatent + lane * kGroup);
-    const uint4 v0 = __ldg(src);
-    const uint4 v1 = __ldg(src + 1);
-    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    float x[16];
+  for (int64_t n0 = warp_global; n0 < n_tokens; n0 += kUnroll * warp_stride) {
+    int64_t slot[kUnroll];
+    uint4 v0[kUnroll], v1[kUnroll];
+    uint32_t rope2[kUnroll];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      x[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
-      x[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
-    }
-    const uint32_t rope2 = __ldg(reinterpret_cast<const uint32_t*>(rope + n * kRope) + lane);
-    const uint32_t rope_e4m3x2 = f32x2_to_e4m3x2(bf16_bits_to_f32(rope2 >> 16), bf16_bits_to_f32(rope2 & 0xFFFFu));
-
-    if constexpr (FMT == 0) {
-      float amax = 0.f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
-      // S = e4m3(amax / 6): IEEE division, then round-to-nearest-even.
-      const uint32_t s_code = f32x2_to_e4m3x2(0.f, __fdiv_rn(amax, 6.0f)) & 0xFFu;
-      const uint32_t s_f16 = e4m3x2_to_f16x2(s_code) & 0xFFFFu;
-      const float s = __half2float(__ushort_as_half(static_cast<unsigned short>(s_f16)));
-      uint32_t lo = 0, hi = 0;  // 16 codes: element 2i in the low nibble of byte i
-      if (s_code != 0) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          lo |= f32x2_to_e2m1x2(__fdiv_rn(x[2 * i + 1], s), __fdiv_rn(x[2 * i], s)) << (8 * i);
-          hi |= f32x2_to_e2m1x2(__fdiv_rn(x[8 + 2 * i + 1], s), __fdiv_rn(x[8 + 2 * i], s)) << (8 * i);
-        }
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t n = n0 + u * warp_stride;
+      slot[u] = -1;
+      if (n < n_tokens) {
+        slot[u] = __ldg(slot_mapping + n);
+        // 16 latent values of group `lane`, as two 16-byte loads.
+        const uint4* src = reinterpret_cast<const uint4*>(latent + n * kLatent + lane * kGroup);
+        v0[u] = __ldg(src);
+        v1[u] = __ldg(src + 1);
+        rope2[u] = __ldg(reinterpret_cast<const uint32_t*>(rope + n * kRope) + lane);
       }
-      *reinterpret_cast<uint2*>(row + lane * 8) = make_uint2(lo, hi);
-      row[kScaleOff + lane] = static_cast<uint8_t>(s_code);
-      *reinterpret_cast<uint16_t*>(row + kRopeOffNvfp4 + 2 * lane) = static_cast<uint16_t>(rope_e4m3x2);
-    } else {
-      uint32_t b[4];
+    }
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        b[i] = f32x2_to_e4m3x2(x[4 * i + 1], x[4 * i]) | (f32x2_to_e4m3x2(x[4 * i + 3], x[4 * i + 2]) << 16);
-      *reinterpret_cast<uint4*>(row + lane * 16) = make_uint4(b[0], b[1], b[2], b[3]);
-      *reinterpret_cast<uint16_t*>(row + kRopeOffFp8 + 2 * lane) = static_cast<uint16_t>(rope_e4m3x2);
+    for (int u = 0; u < kUnroll; ++u) {
+      if (slot[u] < 0 || slot[u] / kBlock >= num_blocks) continue;  // skipped (warp-uniform)
+      uint8_t* row =
+          pool + (slot[u] / kBlock) * block_stride + (slot[u] % kBlock) * (FMT == 0 ? kRowNvfp4 : kRowFp8);
+      const uint32_t w[8] = {v0[u].x, v0[u].y, v0[u].z, v0[u].w, v1[u].x, v1[u].y, v1[u].z, v1[u].w};
+      float x[16];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        x[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
+        x[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+      }
+      const uint32_t rope_e4m3x2 =
+          f32x2_to_e4m3x2(bf16_bits_to_f32(rope2[u] >> 16), bf16_bits_to_f32(rope2[u] & 0xFFFFu));
+
+      if constexpr (FMT == 0) {
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+        // S = e4m3(amax / 6): IEEE division, then round-to-nearest-even.
+        const uint32_t s_code = f32x2_to_e4m3x2(0.f, __fdiv_rn(amax, 6.0f)) & 0xFFu;
+        const uint32_t s_f16 = e4m3x2_to_f16x2(s_code) & 0xFFFFu;
+        const float s = __half2float(__ushort_as_half(static_cast<unsigned short>(s_f16)));
+        uint32_t lo = 0, hi = 0;  // 16 codes: element 2i in the low nibble of byte i
+        if (s_code != 0) {
+          const float r = __frcp_rn(s);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            lo |= f32x2_to_e2m1x2(div_rn(x[2 * i + 1], s, r), div_rn(x[2 * i], s, r)) << (8 * i);
+            hi |= f32x2_to_e2m1x2(div_rn(x[8 + 2 * i + 1], s, r), div_rn(x[8 + 2 * i], s, r)) << (8 * i);
+          }
+        }
+        *reinterpret_cast<uint2*>(row + lane * 8) = make_uint2(lo, hi);
+        row[kScaleOff + lane] = static_cast<uint8_t>(s_code);
+        *reinterpret_cast<uint16_t*>(row + kRopeOffNvfp4 + 2 * lane) = static_cast<uint16_t>(rope_e4m3x2);
+      } else {
+        uint32_t b[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          b[i] = f32x2_to_e4m3x2(x[4 * i + 1], x[4 * i]) | (f32x2_to_e4m3x2(x[4 * i + 3], x[4 * i + 2]) << 16);
+        *reinterpret_cast<uint4*>(row + lane * 16) = make_uint4(b[0], b[1], b[2], b[3]);
+        *reinterpret_cast<uint16_t*>(row + kRopeOffFp8 + 2 * lane) = static_cast<uint16_t>(rope_e4m3x2);
+      }
     }
   }
 }
@@ -89,44 +118,62 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     index_key_append_kernel(const uint16_t* __restrict__ keys, const int64_t* __restrict__ slot_mapping,
                             int64_t n_tokens, uint8_t* __restrict__ pool, int64_t num_blocks,
                             int64_t block_stride) {
+  constexpr int kUnroll = 4;  // pairs of tokens per warp per iteration: all their loads are issued first
   const int lane = threadIdx.x & 31;
   const int half = lane >> 4;
   const int l16 = lane & 15;
   const int64_t warp_global = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
   const int64_t warp_stride = static_cast<int64_t>(gridDim.x) * kWarpsPerBlock;
-  for (int64_t pair = warp_global; 2 * pair < n_tokens; pair += warp_stride) {
-    const int64_t n = 2 * pair + half;
-    const bool in_range = n < n_tokens;
-    const int64_t slot = in_range ? __ldg(slot_mapping + n) : -1;
-    const bool ok = slot >= 0 && slot / kBlock < num_blocks;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (ok) v = __ldg(reinterpret_cast<const uint4*>(keys + n * kIdxDim) + l16);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    float x[8];
+  for (int64_t pair0 = warp_global; 2 * pair0 < n_tokens; pair0 += kUnroll * warp_stride) {
+    int64_t slots[kUnroll];
+    uint4 vs[kUnroll];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      x[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
-      x[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t n = 2 * (pair0 + u * warp_stride) + half;
+      slots[u] = n < n_tokens ? __ldg(slot_mapping + n) : -1;
+      vs[u] = make_uint4(0, 0, 0, 0);
+      if (slots[u] >= 0 && slots[u] / kBlock < num_blocks)
+        vs[u] = __ldg(reinterpret_cast<const uint4*>(keys + n * kIdxDim) + l16);
     }
-    float amax = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    for (int u = 0; u < kUnroll; ++u) {
+      if (2 * (pair0 + u * warp_stride) >= n_tokens) break;  // warp-uniform
+      const int64_t slot = slots[u];
+      const bool ok = slot >= 0 && slot / kBlock < num_blocks;
+      const uint32_t w[4] = {vs[u].x, vs[u].y, vs[u].z, vs[u].w};
+      float x[8];
 #pragma unroll
-    for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-    if (!ok) continue;
-    const float s = amax == 0.f ? 0.f : __fdiv_rn(amax, 448.0f);
-    uint32_t lo = 0, hi = 0;
-    if (amax != 0.f) {
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        lo |= f32x2_to_e4m3x2(__fdiv_rn(x[2 * i + 1], s), __fdiv_rn(x[2 * i], s)) << (16 * i);
-        hi |= f32x2_to_e4m3x2(__fdiv_rn(x[4 + 2 * i + 1], s), __fdiv_rn(x[4 + 2 * i], s)) << (16 * i);
+      for (int i = 0; i < 4; ++i) {
+        x[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
+        x[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
       }
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+      if (!ok) continue;
+      const float s = amax == 0.f ? 0.f : __fdiv_rn(amax, 448.0f);
+      uint32_t lo = 0, hi = 0;
+      if (amax != 0.f && s >= 1.17549435e-38f) {  // normal scale: reciprocal and one correction
+        const float r = __frcp_rn(s);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          lo |= f32x2_to_e4m3x2(div_rn(x[2 * i + 1], s, r), div_rn(x[2 * i], s, r)) << (16 * i);
+          hi |= f32x2_to_e4m3x2(div_rn(x[4 + 2 * i + 1], s, r), div_rn(x[4 + 2 * i], s, r)) << (16 * i);
+        }
+      } else if (amax != 0.f) {  // subnormal scale (1/s overflows): plain IEEE division
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          lo |= f32x2_to_e4m3x2(__fdiv_rn(x[2 * i + 1], s), __fdiv_rn(x[2 * i], s)) << (16 * i);
+          hi |= f32x2_to_e4m3x2(__fdiv_rn(x[4 + 2 * i + 1], s), __fdiv_rn(x[4 + 2 * i], s)) << (16 * i);
+        }
+      }
+      uint8_t* blk = pool + (slot / kBlock) * block_stride;
+      const int64_t o = slot % kBlock;
+      *reinterpret_cast<uint2*>(blk + o * kIdxDim + 8 * l16) = make_uint2(lo, hi);
+      if (l16 == 0) *reinterpret_cast<float*>(blk + static_cast<int64_t>(kBlock) * kIdxDim + 4 * o) = s;
     }
-    uint8_t* blk = pool + (slot / kBlock) * block_stride;
-    const int64_t o = slot % kBlock;
-    *reinterpret_cast<uint2*>(blk + o * kIdxDim + 8 * l16) = make_uint2(lo, hi);
-    if (l16 == 0) *reinterpret_cast<float*>(blk + static_cast<int64_t>(kBlock) * kIdxDim + 4 * o) = s;
   }
 }
 

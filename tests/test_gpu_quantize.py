@@ -136,3 +136,38 @@ def test_append_turn_full_size(fmt):
     untouched = (wl.block_table[:, :100].to(torch.int64) * stride).view(-1)[:500]
     probe = pool[(untouched[:, None] + torch.arange(rb, device=DEV)[None, :]).view(-1)]
     assert int(probe.count_nonzero()) == 0
+
+
+def test_nvfp4_every_value_under_every_scale():
+    """Exhaustive over the code decision x / S: for every positive finite e4m3
+    scale S, groups whose maximum is exactly 6 S (so the group's scale is S)
+    carry every finite bf16 value x with |x| <= 6 S, both signs."""
+    m = lib()
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = O.bf16_to_f64(bits)
+    fin = np.isfinite(vals)
+    bits, vals = bits[fin], vals[fin]
+    groups = []
+    for sc in range(1, 0x7F):
+        S = O.e4m3_decode(sc)
+        amax = 6.0 * S
+        amax_bits = (np.array([amax], np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        assert O.bf16_to_f64(amax_bits)[0] == amax
+        xs = bits[np.abs(vals) <= amax]
+        pad = (-xs.size) % 15
+        xs = np.concatenate([xs, np.zeros(pad, np.uint16)]).reshape(-1, 15)
+        groups.append(np.concatenate([np.repeat(amax_bits[None, :], xs.shape[0], 0), xs], axis=1))
+    g = np.concatenate(groups)                       # [G, 16]
+    pad = (-g.shape[0]) % 32
+    g = np.concatenate([g, np.zeros((pad, 16), np.uint16)])
+    lat_np = g.reshape(-1, 512)
+    n = lat_np.shape[0]
+    rope_np = np.zeros((n, 64), np.uint16)
+    lat = rows_from_bits(lat_np, 512)
+    rope = rows_from_bits(rope_np, 64)
+    nb = -(-n // 64)
+    slots = torch.arange(n, dtype=torch.int64, device=DEV)
+    got, stride = gpu_append(m, lat, rope, slots, nb, O.FMT_NVFP4)
+    want = oracle_pool(lat, rope, slots, nb, O.FMT_NVFP4, stride)
+    bad = np.flatnonzero(got != want)
+    assert bad.size == 0, f"{bad.size} bytes differ (rows {np.unique(bad // 352)[:5]})"

@@ -35,7 +35,7 @@ def bf16_keys(n, seed, spread=10.0):
     return keys
 
 
-@pytest.mark.parametrize("n,nb,pad", [(1, 1, 0), (5, 2, 16), (3000, 60, 0), (20_000, 400, 32)])
+@pytest.mark.parametrize("n,nb,pad", [(1, 1, 0), (5, 2, 16), (3000, 60, 0), (20_000, 400, 32), (300_000, 5000, 0)])
 def test_index_key_append_bit_exact(n, nb, pad):
     m = lib()
     rng = np.random.default_rng(n)
