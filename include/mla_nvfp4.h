@@ -293,7 +293,10 @@ mla_status_t mla_sparse_decode_staged(const uint16_t* q_nope, const uint16_t* q_
  *   scores        device float, request b at scores + b * score_row_stride
  *   topk_out      device int32 [batch, topk]
  *   topk          1..2048
- *   workspace     device, at least mla_topk_workspace_size(...) bytes
+ *   workspace     device, 256-byte aligned, at least
+ *                 mla_topk_workspace_size(...) bytes (candidate lists of
+ *                 the parallel collection pass); contents on entry do not
+ *                 matter
  */
 size_t mla_topk_workspace_size(int batch, int max_context_len, int topk);
 mla_status_t mla_topk(const float* scores, int64_t score_row_stride, const int32_t* context_lens, int batch,

@@ -13,15 +13,18 @@
 // per-token scale, relu and head weights and reduces over heads with two
 // shuffles.  HBM-bound at 132 bytes per token.
 //
-// topk_kernel: one 1,024-thread CTA per request.  Scores map to order-
-// preserving 32-bit keys (with -0.0 folded into +0.0).  A sorted strided
-// sample of 2,048 keys picks a threshold expected to keep ~2.5 k elements; one
-// pass over the row collects the elements at or above it into per-warp lists
-// in index order; three histogram passes over 11 + 11 + 10 key bits then find
-// the k-th largest key T among the candidates and how many ties at T are
-// taken, and an ordered compaction writes every index with key > T and the
-// lowest-index ties in ascending order.  If the threshold keeps too few or
-// too many elements, the same selection runs over the whole row instead.
+// Top-k in two kernels.  Scores map to order-preserving 32-bit keys (with
+// -0.0 folded into +0.0).  topk_collect_kernel: 8 CTAs per request each draw
+// the same strided sample of 2,048 keys of the whole row, take from it a
+// threshold expected to keep ~2.5 k elements (two radix passes over the
+// sample), and collect the elements of their eighth of the row at or above
+// it into global lists in index order.  topk_kernel: one 1,024-thread CTA
+// per request concatenates the 8 lists in order; three histogram passes over
+// 11 + 11 + 10 key bits find the k-th largest key T among the candidates and
+// how many ties at T are taken, and an ordered compaction writes every index
+// with key > T and the lowest-index ties in ascending order.  If the
+// threshold kept too few or too many elements, the same selection runs over
+// the whole row instead.
 #include <cuda_fp16.h>
 
 #include "mla_device.cuh"
@@ -475,118 +478,209 @@ struct CandSrc {
   __device__ int32_t idx(int j) const { return sm->cand_idx[j]; }
 };
 
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restrict__ scores, int64_t row_stride,
-                                                            const int32_t* __restrict__ ctx_lens, int topk,
-                                                            int max_ctx, int32_t* __restrict__ out) {
-  extern __shared__ __align__(16) uint8_t topk_smem_raw[];
-  TopkSmem& sm = *reinterpret_cast<TopkSmem*>(topk_smem_raw);
-  const int b = blockIdx.x;
-  const int n = max(0, min(__ldg(ctx_lens + b), max_ctx));
-  const float* row = scores + static_cast<int64_t>(b) * row_stride;
-  int32_t* orow = out + static_cast<int64_t>(b) * topk;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// ---- parallel candidate collection: kParts CTAs per request ---------------
+// Every part CTA draws the same strided sample of the whole row and takes
+// the same threshold T0 from it (two radix passes over the sample give the
+// lower bound of the 22-bit key bin holding the sample's r0-th largest key);
+// it then collects its part's elements with key >= T0, in index order, into
+// global memory.  The selection kernel concatenates the parts in order.
+constexpr int kParts = 8;
+constexpr int kPartThreads = 256;
+constexpr int kPartWarps = kPartThreads / 32;
+constexpr int kPartCap = kCandCap / kParts;          // 2,048 candidates per part
+constexpr int kPartWarpCap = kPartCap / kPartWarps;  // 256 per warp
 
-  if (n <= topk) {  // everything is selected
-    for (int j = tid; j < topk; j += kTopkThreads) orow[j] = j < n ? j : -1;
-    return;
+struct CollectSmem {
+  uint32_t hist[kHistBins];
+  uint32_t cand_key[kPartCap];
+  int32_t cand_idx[kPartCap];
+  uint32_t scan[kPartWarps];
+  uint32_t warp_cnt[kPartWarps];
+  uint32_t sel_bin, sel_need;
+};
+
+// The bin holding the need-th largest element of hist[] (descending), with
+// 256 threads owning 8 bins each; *need_in_bin as in select_bin.
+__device__ __forceinline__ uint32_t select_bin_256(const uint32_t* hist, uint32_t need, CollectSmem& sm) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  uint32_t h[8], sum = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    h[k] = hist[kHistBins - 1 - 8 * t - k];
+    sum += h[k];
   }
-
-  // 1. Strided sample, sorted descending (bitonic, one pair per thread).
-  for (int i = tid; i < kSample; i += kTopkThreads)
-    sm.sample[i] = order_key(__ldg(row + static_cast<int>((static_cast<int64_t>(i) * n) / kSample)));
+  uint32_t x = sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) sm.scan[warp] = x;
   __syncthreads();
-  for (int size = 2; size <= kSample; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      const int i = 2 * tid - (tid & (stride - 1));  // lower index of this thread's pair
-      const int j = i + stride;
-      const bool desc = (i & size) == 0;             // direction of this sub-sequence
-      const uint32_t a = sm.sample[i], c = sm.sample[j];
-      if ((a < c) == desc) {
-        sm.sample[i] = c;
-        sm.sample[j] = a;
-      }
-      __syncthreads();
+  uint32_t acc = x - sum;
+  for (int w = 0; w < warp; ++w) acc += sm.scan[w];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    if (acc < need && acc + h[k] >= need) {
+      sm.sel_bin = kHistBins - 1 - 8 * t - k;
+      sm.sel_need = need - acc;
     }
+    acc += h[k];
+  }
+  __syncthreads();
+  return sm.sel_bin;
+}
+
+__global__ void __launch_bounds__(kPartThreads)
+    topk_collect_kernel(const float* __restrict__ scores, int64_t row_stride, const int32_t* __restrict__ ctx_lens,
+                        int topk, int max_ctx, uint32_t* __restrict__ cand_key, int32_t* __restrict__ cand_idx,
+                        int32_t* __restrict__ cand_cnt) {
+  __shared__ CollectSmem sm;
+  const int part = blockIdx.x, b = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = max(0, min(__ldg(ctx_lens + b), max_ctx));
+  if (n <= topk) return;  // the selection kernel takes everything
+  const float* row = scores + static_cast<int64_t>(b) * row_stride;
+
+  // 1. Threshold from the strided sample of the whole row.
+  uint32_t key[kSample / kPartThreads];
+#pragma unroll
+  for (int u = 0; u < kSample / kPartThreads; ++u) {
+    const int i = tid + u * kPartThreads;
+    key[u] = order_key(__ldg(row + static_cast<int>((static_cast<int64_t>(i) * n) / kSample)));
   }
   const int r0 = min(kSample - 1, static_cast<int>((2.5 * topk * kSample) / n) + 8);
-  const uint32_t T0 = sm.sample[r0];
+  uint32_t need = r0 + 1, prefix = 0;
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+    for (int j = tid; j < kHistBins; j += kPartThreads) sm.hist[j] = 0;
+    if (tid == 0) sm.sel_bin = sm.sel_need = 0;
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kSample / kPartThreads; ++u) {
+      if (pass == 0) hist_add(sm.hist, key[u] >> 21, true);
+      else hist_add(sm.hist, (key[u] >> 10) & 0x7FFu, (key[u] >> 21) == prefix);
+    }
+    __syncthreads();
+    const uint32_t bin = select_bin_256(sm.hist, need, sm);
+    need = sm.sel_need;
+    prefix = pass == 0 ? bin : ((prefix << 11) | bin);
+    __syncthreads();
+  }
+  const uint32_t T0 = prefix << 10;  // lower bound of the selected 22-bit bin
 
-  // 2. Collect elements >= T0, order-preserving per warp chunk.
-  const int chunk = (n + kTopkWarps - 1) / kTopkWarps;
-  const int lo = warp * chunk, hi = min(n, lo + chunk);
+  // 2. Collect this part's elements >= T0, order-preserving per warp chunk.
+  const int chunk = (n + kParts - 1) / kParts;
+  const int lo = part * chunk, hi = min(n, lo + chunk);
+  const int wchunk = (max(0, hi - lo) + kPartWarps - 1) / kPartWarps;
+  const int wlo = lo + warp * wchunk, whi = min(hi, wlo + wchunk);
   uint32_t cnt = 0;
   constexpr int kBatch = 8;  // independent loads in flight per lane
-  for (int base = lo; base < hi; base += 32 * kBatch) {
-    uint32_t key[kBatch];
+  for (int base = wlo; base < whi; base += 32 * kBatch) {
+    uint32_t k[kBatch];
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int j = base + 32 * u + lane;
-      key[u] = j < hi ? order_key(__ldg(row + j)) : 0u;
+      k[u] = j < whi ? order_key(__ldg(row + j)) : 0u;
     }
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int j = base + 32 * u + lane;
-      const bool take = j < hi && key[u] >= T0;
+      const bool take = j < whi && k[u] >= T0;
       const uint32_t m = __ballot_sync(0xFFFFFFFFu, take);
       const uint32_t pos = cnt + __popc(m & ((1u << lane) - 1u));
-      if (take && pos < kWarpCap) {
-        sm.cand_key[warp * kWarpCap + pos] = key[u];
-        sm.cand_idx[warp * kWarpCap + pos] = j;
+      if (take && pos < kPartWarpCap) {
+        sm.cand_key[warp * kPartWarpCap + pos] = k[u];
+        sm.cand_idx[warp * kPartWarpCap + pos] = j;
       }
       cnt += __popc(m);
     }
   }
   if (lane == 0) sm.warp_cnt[warp] = cnt;
   __syncthreads();
-  uint32_t total = 0, overflow = 0, my_off = 0;
-#pragma unroll 1
-  for (int w = 0; w < kTopkWarps; ++w) {
-    const uint32_t cw = sm.warp_cnt[w];
-    if (w == warp) my_off = total;
-    total += cw;
-    overflow |= cw > static_cast<uint32_t>(kWarpCap);
+  uint32_t off = 0, total = 0;
+  bool overflow = false;
+  for (int w = 0; w < kPartWarps; ++w) {
+    if (w == warp) off = total;
+    total += sm.warp_cnt[w];
+    overflow |= sm.warp_cnt[w] > static_cast<uint32_t>(kPartWarpCap);
   }
-  if (overflow || total < static_cast<uint32_t>(topk)) {
-    // Rare: fall back to exact selection over the whole row.
+  const int64_t slot = static_cast<int64_t>(b) * kParts + part;
+  if (overflow) {
+    if (tid == 0) cand_cnt[slot] = -1;  // the selection kernel falls back to the whole row
+    return;
+  }
+  for (uint32_t e = lane; e < cnt; e += 32) {
+    cand_key[slot * kPartCap + off + e] = sm.cand_key[warp * kPartWarpCap + e];
+    cand_idx[slot * kPartCap + off + e] = sm.cand_idx[warp * kPartWarpCap + e];
+  }
+  if (tid == 0) cand_cnt[slot] = static_cast<int32_t>(total);
+}
+
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restrict__ scores, int64_t row_stride,
+                                                            const int32_t* __restrict__ ctx_lens, int topk,
+                                                            int max_ctx, const uint32_t* __restrict__ cand_key,
+                                                            const int32_t* __restrict__ cand_idx,
+                                                            const int32_t* __restrict__ cand_cnt,
+                                                            int32_t* __restrict__ out) {
+  extern __shared__ __align__(16) uint8_t topk_smem_raw[];
+  TopkSmem& sm = *reinterpret_cast<TopkSmem*>(topk_smem_raw);
+  const int b = blockIdx.x;
+  const int n = max(0, min(__ldg(ctx_lens + b), max_ctx));
+  const float* row = scores + static_cast<int64_t>(b) * row_stride;
+  int32_t* orow = out + static_cast<int64_t>(b) * topk;
+  const int tid = threadIdx.x;
+
+  if (n <= topk) {  // everything is selected
+    for (int j = tid; j < topk; j += kTopkThreads) orow[j] = j < n ? j : -1;
+    return;
+  }
+  // The parts' candidate lists, concatenated in part order (index order kept).
+  const int64_t slot0 = static_cast<int64_t>(b) * kParts;
+  int cnt[kParts];
+  int total = 0;
+  bool overflow = false;
+#pragma unroll
+  for (int p = 0; p < kParts; ++p) {
+    cnt[p] = __ldg(cand_cnt + slot0 + p);
+    overflow |= cnt[p] < 0;
+    total += max(cnt[p], 0);
+  }
+  if (overflow || total < topk) {
+    // Rare: the sample threshold kept too many or too few: exact selection
+    // over the whole row.
     select_and_compact(RowSrc{row}, n, topk, orow, sm);
     return;
   }
-  if (lane == 0) sm.warp_off[warp] = my_off;
-  __syncthreads();
-
-  // 3. Concatenate the lists in warp order (elements only move down).
-  constexpr int kPerThread = kCandCap / kTopkThreads;
-  uint32_t kk[kPerThread];
-  int32_t ii[kPerThread];
-  int dst[kPerThread];
+  int off = 0;
 #pragma unroll
-  for (int e = 0; e < kPerThread; ++e) {
-    const int srcpos = tid + e * kTopkThreads;
-    const int w = srcpos / kWarpCap, o = srcpos % kWarpCap;
-    dst[e] = (o < static_cast<int>(sm.warp_cnt[w])) ? static_cast<int>(sm.warp_off[w]) + o : -1;
-    kk[e] = sm.cand_key[srcpos];
-    ii[e] = sm.cand_idx[srcpos];
+  for (int p = 0; p < kParts; ++p) {
+    for (int e = tid; e < cnt[p]; e += kTopkThreads) {
+      sm.cand_key[off + e] = __ldg(cand_key + (slot0 + p) * kPartCap + e);
+      sm.cand_idx[off + e] = __ldg(cand_idx + (slot0 + p) * kPartCap + e);
+    }
+    off += cnt[p];
   }
   __syncthreads();
-#pragma unroll
-  for (int e = 0; e < kPerThread; ++e)
-    if (dst[e] >= 0) {
-      sm.cand_key[dst[e]] = kk[e];
-      sm.cand_idx[dst[e]] = ii[e];
-    }
-  __syncthreads();
-
-  // 4. Exact selection among the candidates (all in shared memory).
-  select_and_compact(CandSrc{&sm}, static_cast<int>(total), topk, orow, sm);
+  select_and_compact(CandSrc{&sm}, total, topk, orow, sm);
 }
 
 }  // namespace
 
-size_t topk_workspace_bytes(int, int, int) { return 0; }
+size_t topk_workspace_bytes(int batch, int, int) {
+  if (batch <= 0) return 0;
+  const size_t lists = static_cast<size_t>(batch) * kParts * kPartCap * sizeof(uint32_t);
+  return 2 * ((lists + 255) / 256 * 256) + (static_cast<size_t>(batch) * kParts * sizeof(int32_t) + 255) / 256 * 256;
+}
 
 cudaError_t launch_topk(const float* scores, int64_t row_stride, const int32_t* context_lens, int batch, int topk,
-                        int max_context_len, int32_t* out, void*, cudaStream_t stream) {
+                        int max_context_len, int32_t* out, void* workspace, cudaStream_t stream) {
   if (batch <= 0) return cudaSuccess;
+  if (workspace == nullptr) return cudaErrorInvalidValue;
+  const size_t lists = (static_cast<size_t>(batch) * kParts * kPartCap * sizeof(uint32_t) + 255) / 256 * 256;
+  uint32_t* cand_key = static_cast<uint32_t*>(workspace);
+  int32_t* cand_idx = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + lists);
+  int32_t* cand_cnt = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + 2 * lists);
   static int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -597,8 +691,12 @@ cudaError_t launch_topk(const float* scores, int64_t row_stride, const int32_t* 
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
+  topk_collect_kernel<<<dim3(kParts, batch), kPartThreads, 0, stream>>>(scores, row_stride, context_lens, topk,
+                                                                       max_context_len, cand_key, cand_idx, cand_cnt);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   topk_kernel<<<batch, kTopkThreads, sizeof(TopkSmem), stream>>>(scores, row_stride, context_lens, topk,
-                                                                  max_context_len, out);
+                                                                  max_context_len, cand_key, cand_idx, cand_cnt, out);
   return cudaGetLastError();
 }
 

@@ -359,6 +359,7 @@ mla_status_t mla_topk(const float* scores, int64_t score_row_stride, const int32
   if (!scores || !context_lens || !topk_out) return MLA_ERR_INVALID_ARG;
   if (score_row_stride < max_context_len || !aligned(scores, 4) || !aligned(topk_out, 4)) return MLA_ERR_INVALID_ARG;
   if (workspace_bytes < topk_workspace_bytes(batch, max_context_len, topk)) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  if (!workspace || !aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
   return cuda_status(launch_topk(scores, score_row_stride, context_lens, batch, topk, max_context_len, topk_out,
                                  workspace, reinterpret_cast<cudaStream_t>(stream)));
 }
