@@ -644,6 +644,10 @@ DecodePlan plan_sparse_decode(int batch, int num_heads, int topk) {
   const int max_splits = (topk + kStageRows - 1) / kStageRows;
   const int min_splits = (topk + kMaxRows - 1) / kMaxRows;  // a slice fits the CTA's row tables
   splits = splits < min_splits ? min_splits : (splits > max_splits ? max_splits : splits);
+  // The critical path is the number of 32-row stages per CTA: keep it, but
+  // with as few splits as give it (fewer, fuller CTAs and partials to merge).
+  const int stages = ((topk + splits - 1) / splits + kStageRows - 1) / kStageRows;
+  splits = (topk + stages * kStageRows - 1) / (stages * kStageRows);
   int rows = (topk + splits - 1) / splits;
   rows = (rows + 15) / 16 * 16;
   splits = (topk + rows - 1) / rows;
