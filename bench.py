@@ -55,6 +55,7 @@ def parse():
     p.add_argument("--indexer-batch", type=int, default=64, help="requests in the indexer + top-k sub-benchmark")
     p.add_argument("--only-extras", action="store_true", help="time only the sub-benchmarks (profiling)")
     p.add_argument("--draft-tokens", type=int, default=4, help="query tokens per request in the draft-token timing")
+    p.add_argument("--no-dep", action="store_true", help="skip the 128 x 64-head (DEP rank) decode timing")
     return p.parse_args()
 
 
@@ -597,7 +598,58 @@ def sub_measurements(m, W, dev, stream, args, hbm):
     key_bytes = tokens * 132
     out["indexer_topk"] = {"workload": iw.name, "us": t * 1e6, "tokens_per_s": tokens / t,
                            "key_hbm_gbs": key_bytes / t / 1e9, "frac": key_bytes / t / 1e9 / hbm}
+    del iw, ws
+    torch.cuda.empty_cache()
+    if not args.no_dep:
+        out["dep_rank"] = dep_measurement(m, W, dev, stream, args, hbm)
     return out
+
+
+def dep_measurement(m, W, dev, stream, args, hbm):
+    """All heads on one rank: 128 requests x 64 heads, contexts 8K-1M (24M
+    cached tokens), top-2048, NVFP4.  Each launch is timed alone with CUDA
+    events after an L2 flush (the selected rows of one layer fit in L2)."""
+    import torch
+    _, tf_burst, _, _ = peaks()
+    wl = W.dep_rank_decode(dev)
+
+    def qa(lat, rope, slots, pool, nb, stride, fmt):
+        m.mla_kv_quantize_append(lat, rope, slots, pool, nb, 64, stride, fmt)
+
+    W.fill_pool(wl, 0, qa)
+    B, H, K = wl.batch, wl.heads, wl.topk
+    ws = torch.empty(max(m.mla_sparse_decode_workspace_size(B, H, K), 256), dtype=torch.uint8, device=dev)
+    out_t = torch.empty((B, H, 512), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def run():
+        m.mla_sparse_decode(wl.q_nope, wl.q_rope, wl.pools[0], wl.strides[0], wl.num_blocks, wl.block_table,
+                            wl.context_lens, wl.topk_idx, wl.softmax_scale, out=out_t, workspace=ws, stream=stream)
+
+    total_ms = 0.0
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            run()
+        steps = max(3, args.steps // 4)
+        for _ in range(steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            run()
+            e1.record(stream)
+            e1.synchronize()
+            total_ms += e0.elapsed_time(e1)
+    t = total_ms / steps * 1e-3
+    rows = int((wl.topk_idx >= 0).sum())
+    bytes_ = rows * (ROW_NVFP4 + 4) + B * H * (576 * 2 + 512 * 2 + 4)
+    flops = decode_flops(B, H, K)
+    roof = max(bytes_ / (hbm * 1e9), flops / (tf_burst * 1e12))
+    res = {"workload": wl.name, "us": t * 1e6, "rows_per_s": rows / t, "hbm_gbs": bytes_ / t / 1e9,
+           "tflops": flops / t / 1e12, "tensor_frac_of_bf16_peak": flops / t / 1e12 / tf_burst,
+           "roofline_us": roof * 1e6, "frac_of_roofline_time": roof / t}
+    del wl, flush, ws
+    torch.cuda.empty_cache()
+    return res
 
 
 def cpu_baseline(m, W, dev):

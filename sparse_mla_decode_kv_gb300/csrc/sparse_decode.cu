@@ -154,10 +154,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   // v = (request, query token) pair: queries, list, output and partials are
   // indexed by v; the block table and context length by the request b.
-  const int v = blockIdx.x / args.splits;
+  // The head groups of one slice are adjacent in the grid, so they run
+  // together and all but the first read the slice's rows from L2.
+  const int n_hg = args.num_heads / kHeadsPerCta;
+  const int hg = blockIdx.x % n_hg;
+  const int slice = blockIdx.x / n_hg;
+  const int v = slice / args.splits;
   const int b = v / args.q_len;
-  const int sp = blockIdx.x % args.splits;
-  const int hg = blockIdx.y;
+  const int sp = slice % args.splits;
   const int row_begin = sp * args.rows_per_split;
   const int row_end = min(args.topk, row_begin + args.rows_per_split);
   const int n_rows = max(0, row_end - row_begin);
@@ -611,7 +615,7 @@ cudaError_t launch_variant(const DecodeArgs& a, const CUtensorMap& map, int pair
     configured_device = dev;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(pairs * a.splits, a.num_heads / kHeadsPerCta);
+  cfg.gridDim = dim3(pairs * a.splits * (a.num_heads / kHeadsPerCta));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
