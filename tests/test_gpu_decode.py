@@ -182,3 +182,18 @@ def test_nvfp4_and_fp8_agree_within_quantization_error():
 def test_device_fault_word_is_clear():
     m = lib()
     assert m.mla_device_fault(clear=False) == 0
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_block_stride_not_a_whole_number_of_rows(fmt):
+    """A pool whose block stride is not a multiple of the row size cannot be
+    described to TMA as a tensor of rows; the decode then gathers with
+    16-byte cp.async.  Same results against the oracle."""
+    m = lib()
+    wl = small_workload(3, 32, 700, [5000, 1800, 700], seed=31)
+    W.fill_pool(wl, fmt, quantize_fn(m), pad_stride=16)
+    assert wl.strides[fmt] % O.row_bytes(fmt) != 0
+    out, lse = run_gpu(m, wl, fmt)
+    for b in range(wl.batch):
+        ref, ref_lse = oracle_request(wl, b, fmt)
+        assert_decode_close(out[b], lse[b], ref, ref_lse, f"request {b}")

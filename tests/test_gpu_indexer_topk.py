@@ -165,3 +165,18 @@ def test_chained_indexer_topk_decode_full_size():
                                    dec.softmax_scale)
         if set(idx[b].tolist()) == set(O.topk(ref[b], 2048).tolist()):
             assert_decode_close(out[b], lse[b], r, rl, f"request {b}")
+
+
+def test_indexer_key_stride_not_a_multiple_of_128():
+    """Key blocks 16 bytes apart from the packed layout cannot be TMA tiles;
+    the indexer then loads keys directly.  Same contract as the tiled path."""
+    m = lib()
+    wl = W.indexer_keys(DEV, seed=5, batch=3, n_heads=32, topk=256, ctx_lens=[4000, 1000, 300])
+    pad = wl.key_stride + 16
+    pool = torch.zeros(wl.num_blocks * pad, dtype=torch.uint8, device=DEV)
+    pool.view(wl.num_blocks, pad)[:, :wl.key_stride] = wl.key_pool.view(wl.num_blocks, wl.key_stride)
+    ref = oracle_scores(wl, None, 1)
+    wl.key_pool, wl.key_stride = pool, pad
+    idx, sc = run_indexer(m, wl, 4000)
+    for b in range(3):
+        check_request(idx[b], sc[b], ref[b], wl.topk)

@@ -163,3 +163,31 @@ def test_staged_decode_against_oracle(B, H, k, ctx):
     nat = nat.float().cpu().numpy()
     rel = np.linalg.norm(nat - out) / np.linalg.norm(nat)
     assert 0 < rel < 0.1
+
+
+def test_staged_decode_tp4_full_size_sampled():
+    """The TP4 rank as bench.py times it (32 requests x 16 heads, 140,000-token
+    contexts, top-2048) through the staged path; 3 requests against the
+    oracle's staged copies of the same seeded rows."""
+    import workloads as W
+    m = lib()
+    wl = W.tp4_rank_decode(DEV)
+    W.fill_pool(wl, O.FMT_NVFP4, lambda lat, rope, slots, pool, nb, stride, fmt:
+                m.mla_kv_quantize_append(lat, rope, slots, pool, nb, 64, stride, fmt))
+    lse = torch.empty((wl.batch, wl.heads), dtype=torch.float32, device=DEV)
+    out, _ = m.mla_sparse_decode_staged(wl.q_nope, wl.q_rope, wl.pools[0], wl.strides[0], wl.num_blocks,
+                                        wl.block_table, wl.context_lens, wl.topk_idx, wl.softmax_scale, lse=lse)
+    torch.cuda.synchronize()
+    out, lse = out.float().cpu().numpy(), lse.cpu().numpy()
+    k = wl.topk
+    for b in [0, 13, 31]:
+        lat, rope = wl.request_rows(b, wl.topk_idx[b])
+        lat, rope = u16(lat), u16(rope)
+        staged = np.zeros((k + 63) // 64 * 64 * 576, dtype=np.uint8).reshape(-1, 576)
+        for j in range(k):
+            staged[j] = O.stage_row_fp8(O.quantize_row(lat[j], rope[j], O.FMT_NVFP4))
+        nblk = (k + 63) // 64
+        ref, ref_lse = O.sparse_decode(u16(wl.q_nope[b:b + 1]), u16(wl.q_rope[b:b + 1]), staged.reshape(-1), 64 * 576,
+                                       np.arange(nblk, dtype=np.int32)[None], np.array([nblk * 64], np.int32),
+                                       np.arange(k, dtype=np.int32)[None], 64, wl.softmax_scale, O.FMT_FP8)
+        assert_decode_close(out[b], lse[b], ref[0], ref_lse[0], f"staged request {b}")
