@@ -386,8 +386,8 @@ def main():
         ms_st = timed(graphs[2], args.steps, args.warmup)
         ms_mtp = timed(graphs[3], args.steps, args.warmup)
     clk = clocks.summary()
-    splits = m.mla_sparse_decode_workspace_size(B, H, K) > 0
-    launches_per_step = L * (2 if splits else 1)
+    plan = m.mla_sparse_decode_plan(B, H, K)
+    launches_per_step = L * plan["kernels"]
 
     per_layer4 = ms4 / L * 1e-3
     per_layer8 = ms8 / L * 1e-3
@@ -491,7 +491,10 @@ def main():
         "hbm_gbs": ach4,
         "roofline": {"bound": "hbm" if layer_bytes4 / hbm / 1e9 >= fl / tf_burst / 1e12 else "tensor",
                      "achieved": ach4, "peak": hbm, "unit": "GB/s", "frac": ach4 / hbm, "traffic": decode_traffic(),
-                     "kernel": "sparse_decode_kernel<NVFP4> + splitk_merge_kernel (one decode layer)",
+                     "kernel": ("sparse_decode_kernel<NVFP4>, splits merged inside their cluster (one launch per layer)"
+                                if plan["kernels"] == 1 else
+                                "sparse_decode_kernel<NVFP4> + splitk_merge_kernel (one decode layer)"),
+                     "plan": plan,
                      "algorithmic_bytes_per_launch": layer_bytes4, "peak_source": peak_kind,
                      "roofline_us": roof_t4 * 1e6, "frac_of_roofline_time": roof_t4 / per_layer4,
                      "vs_nominal_8tbs": ach4 / 8000.0},

@@ -146,7 +146,10 @@ mla_status_t mla_index_key_quantize_append(const uint16_t* keys, const int64_t* 
  *
  * An empty V_b gives out = 0 and lse = -inf.  Arithmetic: FP16 tensor-core
  * operands (the dequantized values are exact in FP16; q is converted from
- * bf16 with saturation at +-65504) and FP32 accumulation and softmax.
+ * bf16 with saturation at +-65504) and FP32 accumulation and softmax; when
+ * the list is split over several CTAs (mla_sparse_decode_plan), each split's
+ * normalised partial output is rounded to FP16 in the workspace before the
+ * FP32 LSE-weighted merge.
  *
  *   q_nope        device bf16 [batch, num_heads, 512] (W_UK already absorbed)
  *   q_rope        device bf16 [batch, num_heads, 64]
@@ -165,6 +168,21 @@ mla_status_t mla_index_key_quantize_append(const uint16_t* keys, const int64_t* 
  * batch == 0 is a no-op.
  */
 size_t mla_sparse_decode_workspace_size(int batch, int num_heads, int topk);
+
+/*
+ * How mla_sparse_decode (and the FP8, no-alloc and draft-token variants, the
+ * latter with batch = requests x query tokens) divides one call's work on the
+ * current device.  Each (request, 16-head group) is split along its top-k
+ * list into *splits CTAs of *rows_per_split entries (a multiple of 16); the
+ * splits' partial outputs are combined by their LSEs.  *kernels is the number
+ * of kernels the call launches: 1 for one split, or for 2..8 splits, which
+ * form a thread-block cluster and merge inside the decode kernel; 2 for more
+ * splits, merged by a second kernel.  Output pointers may be NULL.
+ * MLA_ERR_INVALID_ARG for batch < 1, num_heads not a positive multiple of
+ * 16, or topk < 1.
+ */
+mla_status_t mla_sparse_decode_plan(int batch, int num_heads, int topk, int* splits, int* rows_per_split,
+                                    int* kernels);
 mla_status_t mla_sparse_decode(const uint16_t* q_nope, const uint16_t* q_rope, const void* kv_pool,
                                int64_t kv_block_stride, int64_t num_blocks, const int32_t* block_table,
                                int max_blocks_per_req, const int32_t* context_lens, const int32_t* topk_idx,

@@ -17,7 +17,7 @@ import torch
 __all__ = [
     "MlaError", "MLA_KV_NVFP4", "MLA_KV_FP8", "library_path", "load",
     "mla_kv_row_bytes", "mla_status_string", "mla_last_cuda_error", "mla_device_fault",
-    "mla_kv_quantize_append", "mla_sparse_decode_workspace_size", "mla_sparse_decode",
+    "mla_kv_quantize_append", "mla_sparse_decode_workspace_size", "mla_sparse_decode_plan", "mla_sparse_decode",
     "mla_sparse_decode_fp8", "mla_sparse_decode_noalloc", "mla_topk_workspace_size", "mla_topk",
     "mla_indexer_topk_workspace_size", "mla_indexer_topk", "mla_index_key_quantize_append",
     "mla_staged_pool_bytes", "mla_stage_rows_fp8", "mla_sparse_decode_staged_workspace_size",
@@ -42,6 +42,7 @@ SIGNATURES = {
     "mla_device_fault": (_I32, [_P, _I32, _P]),
     "mla_kv_quantize_append": (_I32, [_P, _P, _P, _I64, _P, _I64, _I32, _I64, _I32, _P]),
     "mla_sparse_decode_workspace_size": (_SZ, [_I32, _I32, _I32]),
+    "mla_sparse_decode_plan": (_I32, [_I32, _I32, _I32, _P, _P, _P]),
     "mla_sparse_decode": (_I32, [_P, _P, _P, _I64, _I64, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _F32, _P, _P,
                                  _P, _SZ, _P]),
     "mla_sparse_decode_fp8": (_I32, [_P, _P, _P, _I64, _I64, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _F32, _P,
@@ -189,6 +190,14 @@ def mla_index_key_quantize_append(keys: torch.Tensor, slot_mapping: torch.Tensor
 # --------------------------------------------------------------------- sparse decode
 def mla_sparse_decode_workspace_size(batch: int, num_heads: int, topk: int) -> int:
     return int(load().mla_sparse_decode_workspace_size(batch, num_heads, topk))
+
+
+def mla_sparse_decode_plan(batch: int, num_heads: int, topk: int) -> dict:
+    """{"splits", "rows_per_split", "kernels"} of one decode call on the current device."""
+    sp, rows, kern = C.c_int(0), C.c_int(0), C.c_int(0)
+    _check("mla_sparse_decode_plan",
+           load().mla_sparse_decode_plan(batch, num_heads, topk, C.byref(sp), C.byref(rows), C.byref(kern)))
+    return {"splits": sp.value, "rows_per_split": rows.value, "kernels": kern.value}
 
 
 def _decode(cname: str, q_nope, q_rope, kv_pool, kv_block_stride, num_blocks, block_table, context_lens, topk_idx,

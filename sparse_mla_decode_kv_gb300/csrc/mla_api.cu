@@ -209,6 +209,16 @@ size_t mla_sparse_decode_workspace_size(int batch, int num_heads, int topk) {
   return plan_sparse_decode(batch, num_heads, topk).workspace;
 }
 
+mla_status_t mla_sparse_decode_plan(int batch, int num_heads, int topk, int* splits, int* rows_per_split,
+                                    int* kernels) {
+  if (batch <= 0 || num_heads < 16 || num_heads % 16 != 0 || topk < 1) return MLA_ERR_INVALID_ARG;
+  const DecodePlan plan = plan_sparse_decode(batch, num_heads, topk);
+  if (splits) *splits = plan.splits;
+  if (rows_per_split) *rows_per_split = plan.rows_per_split;
+  if (kernels) *kernels = (plan.splits > 1 && !plan.cluster) ? 2 : 1;
+  return MLA_OK;
+}
+
 mla_status_t mla_sparse_decode(const uint16_t* q_nope, const uint16_t* q_rope, const void* kv_pool,
                                int64_t kv_block_stride, int64_t num_blocks, const int32_t* block_table,
                                int max_blocks_per_req, const int32_t* context_lens, const int32_t* topk_idx,

@@ -41,7 +41,8 @@ cudaError_t launch_stage_rows_fp8(const void* pool, int64_t block_stride, int64_
 struct DecodePlan {
   int splits;          // CTAs per (request, 16-head group) along the top-k list
   int rows_per_split;  // multiple of 16
-  size_t workspace;    // bytes of split partials (0 when splits == 1)
+  bool cluster;        // the splits form a thread-block cluster and merge through DSMEM
+  size_t workspace;    // bytes of split partials in global memory (0 for one split or a cluster merge)
 };
 DecodePlan plan_sparse_decode(int batch, int num_heads, int topk);
 cudaError_t launch_sparse_decode(int fmt, const uint16_t* q_nope, const uint16_t* q_rope, const void* pool,

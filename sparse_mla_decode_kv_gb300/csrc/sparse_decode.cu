@@ -66,6 +66,9 @@ constexpr int kMaxRows = 1024;  // list entries of one CTA's slice (the plan nev
 constexpr int kRedPitch = 24;  // floats per token row of the partial-score exchange
 constexpr int kPPitch = 40;    // halfs per head row of P (80 bytes: ldmatrix conflict-free)
 constexpr int kKSteps = 9;     // k-steps of 16 dims per consumer warp (128 latent + 16 rope)
+// Splits of one (request, head group) up to this many form a thread-block
+// cluster and merge their partials through distributed shared memory.
+constexpr int kMaxClusterSplits = 8;
 // Lazy softmax maximum: scores are exponentiated against a reference maximum
 // that is raised only when a score exceeds it by more than kLazy (base 2), so
 // P stays <= 2^kLazy (fine in f16) and the common path needs no reduction.
@@ -105,6 +108,8 @@ struct alignas(128) Smem {
   int rescale[kConsumerWarps];
   float mfin[kHeadsPerCta];
   float lfin[kHeadsPerCta];
+  float mw[kHeadsPerCta][kMaxClusterSplits];  // cluster merge: split weights per head
+  float minv[kHeadsPerCta];                   // cluster merge: 1 / sum of a head's weights
   int64_t row_off[kMaxRows];  // per row of the slice: byte offset in the pool (TMA: row index), -1 if masked
   int32_t tok_all[kMaxRows];  // token of each row of the slice, -1 if masked
   uint64_t full[Fmt<FMT>::kStages];
@@ -122,7 +127,7 @@ struct DecodeArgs {
   const int32_t* topk_idx;
   uint16_t* out;
   float* lse;
-  float* part_o;    // [B*H, splits, 512] (splits > 1)
+  __half* part_o;   // [B*H, splits, 512] normalised partial O in f16 (splits > 1)
   float* part_lse;  // [B*H, splits], base-2
   int max_blocks;
   int topk;
@@ -130,12 +135,100 @@ struct DecodeArgs {
   int num_heads;
   int splits;
   int rows_per_split;
+  int cluster_merge;  // 1: the splits of a (request, head group) are one cluster, merged through DSMEM
   float scale_log2;  // softmax_scale * log2(e)
   unsigned int* fault_word;
 };
 
+// Two floats to f16 (round to nearest even), `lo` in the low half.
+__device__ __forceinline__ uint32_t half2_bits(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ float2 half2_floats(uint32_t bits) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&bits));
+}
+
 __device__ __forceinline__ uint32_t bf16pair_to_f16x2(uint32_t two) {
   return f32x2_to_f16x2_sat(bf16_bits_to_f32(two & 0xFFFFu), bf16_bits_to_f32(two >> 16));
+}
+
+// Cluster merge: the splits of one (request, head group) are the CTAs of a
+// cluster.  Each has written its normalised partial O and base-2 LSE to the
+// workspace (through L2: distributed shared memory has a fraction of L2's
+// bandwidth per SM); after the cluster barrier (release/acquire at cluster
+// scope) CTA r combines the float4 units r*128 + t + k*S*128 of the 16 x 512
+// output tile from every split: LSE = log2 sum_r 2^lse_r and
+// out = sum_r 2^(lse_r - max) O_r / sum_r 2^(lse_r - max).
+template <typename SmemT>
+__device__ __forceinline__ void cluster_merge(const DecodeArgs& args, SmemT& sm, int v, int hg, int sp) {
+  cluster_sync_all();
+  const int S = args.splits;
+  const int64_t bh_base = static_cast<int64_t>(v) * args.num_heads + hg * kHeadsPerCta;
+  // split weights per head: thread t < 16 S reads the LSE of head t / S from
+  // split t % S, then thread h < 16 turns head h's into weights
+  if (static_cast<int>(threadIdx.x) < kHeadsPerCta * S) {
+    const int h = threadIdx.x / S, r = threadIdx.x % S;
+    sm.mw[h][r] = __ldcg(args.part_lse + (bh_base + h) * S + r);
+  }
+  named_bar_sync(1, kThreads);
+  if (threadIdx.x < kHeadsPerCta) {
+    const int h = threadIdx.x;
+    float mx = -INFINITY;
+    for (int r = 0; r < S; ++r) mx = fmaxf(mx, sm.mw[h][r]);
+    float wsum = 0.f;
+    for (int r = 0; r < S; ++r) {
+      const float ws = mx == -INFINITY ? 0.f : ex2(sm.mw[h][r] - mx);  // 0 for an empty split
+      sm.mw[h][r] = ws;
+      wsum += ws;
+    }
+    sm.minv[h] = wsum > 0.f ? 1.f / wsum : 0.f;
+    if (args.lse != nullptr && h % S == sp) args.lse[bh_base + h] = wsum > 0.f ? (mx + lg2(wsum)) * kLn2 : -INFINITY;
+  }
+  named_bar_sync(1, kThreads);
+  // unit u = (head u / 64, dims 8 (u % 64) .. + 8) of the 16 x 512 tile
+  constexpr int kPerHead = kLatent / 8;
+  constexpr int kUnits = kHeadsPerCta * kPerHead;
+  const uint4* part = reinterpret_cast<const uint4*>(args.part_o);
+  for (int u0 = sp * kThreads + static_cast<int>(threadIdx.x); u0 < kUnits; u0 += 2 * S * kThreads) {
+    uint4 pv[2][kMaxClusterSplits];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int u = u0 + i * S * kThreads;
+      const int64_t row = (bh_base + u / kPerHead) * S;
+#pragma unroll
+      for (int r = 0; r < kMaxClusterSplits; ++r)
+        pv[i][r] = (u < kUnits && r < S) ? __ldcg(part + (row + r) * kPerHead + u % kPerHead) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int u = u0 + i * S * kThreads;
+      if (u < kUnits) {
+        const int h = u / kPerHead;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int r = 0; r < kMaxClusterSplits; ++r) {
+          const float ws = r < S ? sm.mw[h][r] : 0.f;
+          const uint32_t wd[4] = {pv[i][r].x, pv[i][r].y, pv[i][r].z, pv[i][r].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 f = half2_floats(wd[k]);
+            acc[2 * k] += ws * f.x;
+            acc[2 * k + 1] += ws * f.y;
+          }
+        }
+        const float inv = sm.minv[h];
+        uint32_t ob[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const __nv_bfloat162 x = __floats2bfloat162_rn(acc[2 * k] * inv, acc[2 * k + 1] * inv);
+          ob[k] = *reinterpret_cast<const uint32_t*>(&x);
+        }
+        *reinterpret_cast<uint4*>(args.out + (bh_base + h) * kLatent + 8 * (u % kPerHead)) =
+            make_uint4(ob[0], ob[1], ob[2], ob[3]);
+      }
+    }
+  }
 }
 
 // TMA = true: rows are gathered by TMA, 4 rows per instruction (the pool's
@@ -156,12 +249,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // indexed by v; the block table and context length by the request b.
   // The head groups of one slice are adjacent in the grid, so they run
   // together and all but the first read the slice's rows from L2.
+  // Cluster merge: the splits of one (request, head group) are adjacent
+  // instead, and the split index is the CTA's rank in its cluster.
   const int n_hg = args.num_heads / kHeadsPerCta;
-  const int hg = blockIdx.x % n_hg;
-  const int slice = blockIdx.x / n_hg;
-  const int v = slice / args.splits;
+  const int hg = args.cluster_merge ? (blockIdx.x / args.splits) % n_hg : blockIdx.x % n_hg;
+  const int v = args.cluster_merge ? blockIdx.x / (args.splits * n_hg) : blockIdx.x / (n_hg * args.splits);
   const int b = v / args.q_len;
-  const int sp = slice % args.splits;
+  const int sp = args.cluster_merge ? blockIdx.x % args.splits : (blockIdx.x / n_hg) % args.splits;
   const int row_begin = sp * args.rows_per_split;
   const int row_end = min(args.topk, row_begin + args.rows_per_split);
   const int n_rows = max(0, row_end - row_begin);
@@ -484,7 +578,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int it2 = abort_it; it2 < next_fill; ++it2)
         mbar_wait_bounded(&sm.full[it2 % kStages], static_cast<uint32_t>(it2 / kStages) & 1u, args.fault_word,
                           kFaultDecodeWait);
-    return;
+    if (!args.cluster_merge) return;
+    // Every CTA of a cluster must reach the cluster barrier: this one joins
+    // the merge as an empty split.
+#pragma unroll
+    for (int e = 0; e < 4; ++e) l_run[e] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+      for (int be = 0; be < 2; ++be)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[ks][be][e] = 0.f;
   }
 
   // ---------------------------------------------------------------- finish
@@ -531,31 +635,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       args.lse[bh1] = lse2_1 * kLn2;
     }
   } else {
-    float* p0 = args.part_o + (bh0 * args.splits + sp) * kLatent;
-    float* p1 = args.part_o + (bh1 * args.splits + sp) * kLatent;
+    // The normalised partial is a convex combination of dequantised values
+    // (|x| <= 6 x 448), so f16 holds it with 11 significant bits.
+    __half* p0 = args.part_o + (bh0 * args.splits + sp) * kLatent;
+    __half* p1 = args.part_o + (bh1 * args.splits + sp) * kLatent;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int dim = 128 * w + 32 * q + 8 * c;
-      *reinterpret_cast<float4*>(p0 + dim) = make_float4(o[2 * q][0][0] * inv0, o[2 * q][0][1] * inv0,
-                                                        o[2 * q][1][0] * inv0, o[2 * q][1][1] * inv0);
-      *reinterpret_cast<float4*>(p0 + dim + 4) = make_float4(o[2 * q + 1][0][0] * inv0, o[2 * q + 1][0][1] * inv0,
-                                                            o[2 * q + 1][1][0] * inv0, o[2 * q + 1][1][1] * inv0);
-      *reinterpret_cast<float4*>(p1 + dim) = make_float4(o[2 * q][0][2] * inv1, o[2 * q][0][3] * inv1,
-                                                        o[2 * q][1][2] * inv1, o[2 * q][1][3] * inv1);
-      *reinterpret_cast<float4*>(p1 + dim + 4) = make_float4(o[2 * q + 1][0][2] * inv1, o[2 * q + 1][0][3] * inv1,
-                                                            o[2 * q + 1][1][2] * inv1, o[2 * q + 1][1][3] * inv1);
+      *reinterpret_cast<uint4*>(p0 + dim) =
+          make_uint4(half2_bits(o[2 * q][0][0] * inv0, o[2 * q][0][1] * inv0),
+                     half2_bits(o[2 * q][1][0] * inv0, o[2 * q][1][1] * inv0),
+                     half2_bits(o[2 * q + 1][0][0] * inv0, o[2 * q + 1][0][1] * inv0),
+                     half2_bits(o[2 * q + 1][1][0] * inv0, o[2 * q + 1][1][1] * inv0));
+      *reinterpret_cast<uint4*>(p1 + dim) =
+          make_uint4(half2_bits(o[2 * q][0][2] * inv1, o[2 * q][0][3] * inv1),
+                     half2_bits(o[2 * q][1][2] * inv1, o[2 * q][1][3] * inv1),
+                     half2_bits(o[2 * q + 1][0][2] * inv1, o[2 * q + 1][0][3] * inv1),
+                     half2_bits(o[2 * q + 1][1][2] * inv1, o[2 * q + 1][1][3] * inv1));
     }
     if (w == 0 && c == 0) {
       args.part_lse[bh0 * args.splits + sp] = lse2_0;
       args.part_lse[bh1 * args.splits + sp] = lse2_1;
     }
+    if (args.cluster_merge) cluster_merge(args, sm, v, hg, sp);
   }
 }
 
 // Combine `splits` normalised partial outputs with their base-2 LSEs:
 // LSE = log2 sum_s 2^lse_s, out = sum_s 2^(lse_s - LSE) * O_s.  One CTA per
-// (request, head); thread i handles dims [4i, 4i+4).
-__global__ void __launch_bounds__(128) splitk_merge_kernel(const float* __restrict__ part_o,
+// (request, head); thread i handles dims [4i, 4i+4).  The partials are read
+// in chunks of kMergeChunk splits whose loads are all issued before any is
+// used (one L2 round trip per chunk, not per split); a running maximum
+// rescales the sums between chunks.
+constexpr int kMergeChunk = 8;
+__global__ void __launch_bounds__(128) splitk_merge_kernel(const __half* __restrict__ part_o,
                                                            const float* __restrict__ part_lse, int splits,
                                                            uint16_t* __restrict__ out, float* __restrict__ lse) {
   // Launched as a programmatic dependent of the decode: wait until that grid
@@ -566,20 +679,40 @@ __global__ void __launch_bounds__(128) splitk_merge_kernel(const float* __restri
   const int64_t bh = blockIdx.x;
   const int t = threadIdx.x;
   const float* pl = part_lse + bh * splits;
+  const uint2* src = reinterpret_cast<const uint2*>(part_o + bh * splits * kLatent) + t;
   float mx = -INFINITY;
-  for (int s = 0; s < splits; ++s) mx = fmaxf(mx, __ldg(pl + s));
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
-  if (mx != -INFINITY) {
-    const float4* src = reinterpret_cast<const float4*>(part_o + bh * splits * kLatent) + t;
-    for (int s = 0; s < splits; ++s) {
-      const float ws = ex2(__ldg(pl + s) - mx);
-      const float4 v = __ldg(src + s * (kLatent / 4));
+  for (int s0 = 0; s0 < splits; s0 += kMergeChunk) {
+    float ls[kMergeChunk];
+    float4 v[kMergeChunk];
+#pragma unroll
+    for (int u = 0; u < kMergeChunk; ++u) {
+      const bool in = s0 + u < splits;
+      ls[u] = in ? __ldg(pl + s0 + u) : -INFINITY;
+      const uint2 hv = in ? __ldg(src + (s0 + u) * (kLatent / 4)) : make_uint2(0, 0);
+      const float2 a = half2_floats(hv.x), b = half2_floats(hv.y);
+      v[u] = make_float4(a.x, a.y, b.x, b.y);
+    }
+    float cm = mx;
+#pragma unroll
+    for (int u = 0; u < kMergeChunk; ++u) cm = fmaxf(cm, ls[u]);
+    if (cm == -INFINITY) continue;  // nothing selected so far
+    const float al = ex2(mx - cm);  // 0 while mx is -inf
+    wsum *= al;
+    acc.x *= al;
+    acc.y *= al;
+    acc.z *= al;
+    acc.w *= al;
+    mx = cm;
+#pragma unroll
+    for (int u = 0; u < kMergeChunk; ++u) {
+      const float ws = ex2(ls[u] - mx);  // 0 for an empty split (lse -inf)
       wsum += ws;
-      acc.x += ws * v.x;
-      acc.y += ws * v.y;
-      acc.z += ws * v.z;
-      acc.w += ws * v.w;
+      acc.x += ws * v[u].x;
+      acc.y += ws * v[u].y;
+      acc.z += ws * v[u].z;
+      acc.w += ws * v[u].w;
     }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
@@ -619,11 +752,15 @@ cudaError_t launch_variant(const DecodeArgs& a, const CUtensorMap& map, int pair
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = a.cluster_merge ? static_cast<unsigned>(a.splits) : 1u;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = a.cluster_merge ? 2 : 1;
   e = cudaLaunchKernelEx(&cfg, sparse_decode_kernel<FMT, TMA>, a, map);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -641,7 +778,7 @@ cudaError_t launch_fmt(const DecodeArgs& a, int pairs, cudaStream_t stream) {
 }  // namespace
 
 DecodePlan plan_sparse_decode(int batch, int num_heads, int topk) {
-  DecodePlan p{1, 0, 0};
+  DecodePlan p{1, 0, false, 0};
   const int groups = batch * (num_heads / kHeadsPerCta);
   const int slots = 2 * device_sm_count();  // two CTAs per SM fit (registers, shared memory)
   int splits = groups > 0 ? slots / groups : 1;
@@ -657,9 +794,10 @@ DecodePlan plan_sparse_decode(int batch, int num_heads, int topk) {
   splits = (topk + rows - 1) / rows;
   p.splits = splits;
   p.rows_per_split = rows;
+  p.cluster = splits > 1 && splits <= kMaxClusterSplits;
   if (splits > 1) {
     const size_t n_bh = static_cast<size_t>(batch) * num_heads;
-    size_t o_bytes = n_bh * splits * kLatent * sizeof(float);
+    size_t o_bytes = n_bh * splits * kLatent * sizeof(__half);
     o_bytes = (o_bytes + 255) / 256 * 256;
     p.workspace = o_bytes + ((n_bh * splits * sizeof(float) + 255) / 256 * 256);
   }
@@ -690,6 +828,7 @@ cudaError_t launch_sparse_decode(int fmt, const uint16_t* q_nope, const uint16_t
   a.num_heads = num_heads;
   a.splits = plan.splits;
   a.rows_per_split = plan.rows_per_split;
+  a.cluster_merge = plan.cluster ? 1 : 0;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.part_o = nullptr;
   a.part_lse = nullptr;
@@ -697,13 +836,13 @@ cudaError_t launch_sparse_decode(int fmt, const uint16_t* q_nope, const uint16_t
   if (a.fault_word == nullptr) return cudaErrorInvalidDevicePointer;
   if (plan.splits > 1) {
     const size_t n_bh = static_cast<size_t>(pairs) * num_heads;
-    size_t o_bytes = n_bh * plan.splits * kLatent * sizeof(float);
+    size_t o_bytes = n_bh * plan.splits * kLatent * sizeof(__half);
     o_bytes = (o_bytes + 255) / 256 * 256;
-    a.part_o = static_cast<float*>(workspace);
+    a.part_o = static_cast<__half*>(workspace);
     a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + o_bytes);
   }
   cudaError_t e = fmt == 0 ? launch_fmt<0>(a, pairs, stream) : launch_fmt<1>(a, pairs, stream);
-  if (e != cudaSuccess || plan.splits == 1) return e;
+  if (e != cudaSuccess || plan.splits == 1 || plan.cluster) return e;
   const int64_t n_bh = static_cast<int64_t>(pairs) * num_heads;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(n_bh));
@@ -715,7 +854,7 @@ cudaError_t launch_sparse_decode(int fmt, const uint16_t* q_nope, const uint16_t
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, splitk_merge_kernel, static_cast<const float*>(a.part_o),
+  e = cudaLaunchKernelEx(&cfg, splitk_merge_kernel, static_cast<const __half*>(a.part_o),
                          static_cast<const float*>(a.part_lse), plan.splits, out, lse);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

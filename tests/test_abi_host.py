@@ -113,6 +113,31 @@ def test_topk_and_indexer_validation(lib):
     assert lib.mla_indexer_topk_workspace_size(2, 4096, 2048) >= 2 * 4096 * 4
 
 
+def test_split_workspace_holds_every_partial(lib):
+    """Split partials (normalised O in f16 and a float base-2 LSE per split and
+    head) live in the workspace, whether the splits merge inside their
+    thread-block cluster (up to 8) or in a second kernel."""
+    for batch, splits_at_least in [(32, 2), (2, 32)]:
+        need = batch * 16 * splits_at_least * (512 * 2 + 4)
+        assert lib.mla_sparse_decode_workspace_size(batch, 16, 2048) >= need
+
+
+def test_decode_plan(lib):
+    """The plan query agrees with the workspace query and the merge rule (up
+    to 8 splits merge inside their cluster: one kernel)."""
+    import sparse_mla_decode_kv_gb300 as m
+    for batch, heads, topk in [(32, 16, 2048), (2, 16, 2048), (1, 16, 1), (128, 64, 2048), (3, 32, 300)]:
+        p = m.mla_sparse_decode_plan(batch, heads, topk)
+        assert p["rows_per_split"] % 16 == 0 and p["splits"] * p["rows_per_split"] >= topk
+        assert (p["splits"] - 1) * p["rows_per_split"] < topk  # no empty split
+        assert p["kernels"] == (2 if p["splits"] > 8 else 1)
+        assert (lib.mla_sparse_decode_workspace_size(batch, heads, topk) > 0) == (p["splits"] > 1)
+    assert lib.mla_sparse_decode_plan(0, 16, 2048, None, None, None) == 1
+    assert lib.mla_sparse_decode_plan(4, 8, 2048, None, None, None) == 1
+    assert lib.mla_sparse_decode_plan(4, 16, 0, None, None, None) == 1
+    assert lib.mla_sparse_decode_plan(4, 16, 2048, None, None, None) == 0
+
+
 def test_workspace_sizes_are_zero_for_empty_or_invalid(lib):
     assert lib.mla_sparse_decode_workspace_size(0, 16, 2048) == 0
     assert lib.mla_sparse_decode_workspace_size(4, 8, 2048) == 0

@@ -50,11 +50,14 @@ def run_both(m, wl):
 def test_no_alloc_decode_matches_workspace_decode_twice():
     m = lib()
     assert m.mla_sparse_decode_workspace_size(32, 16, 2048) <= 16 << 20
+    # 8 splits (merged inside a thread-block cluster), 32 and 64 splits
+    # (merged by a second kernel)
     cases = [
         build_case(m, lambda: W.tiny_decode(DEV, seed=3)),
         build_case(m, lambda: W.tp4_rank_decode(DEV, seed=5, batch=8, ctx=20_000)),
+        build_case(m, lambda: W.tp4_rank_decode(DEV, seed=6, batch=2, ctx=9_000)),
     ]
-    for wl in cases:  # two calls in a row, different shapes sharing the scratch
+    for wl in cases:  # calls in a row, different shapes sharing the scratch
         assert m.mla_sparse_decode_workspace_size(wl.batch, wl.heads, wl.topk) > 0  # the scratch is used
         (out, lse), (ref, ref_lse) = run_both(m, wl)
         for b in range(wl.batch):
