@@ -108,8 +108,6 @@ struct alignas(128) Smem {
   int rescale[kConsumerWarps];
   float mfin[kHeadsPerCta];
   float lfin[kHeadsPerCta];
-  float mw[kHeadsPerCta][kMaxClusterSplits];  // cluster merge: split weights per head
-  float minv[kHeadsPerCta];                   // cluster merge: 1 / sum of a head's weights
   int64_t row_off[kMaxRows];  // per row of the slice: byte offset in the pool (TMA: row index), -1 if masked
   int32_t tok_all[kMaxRows];  // token of each row of the slice, -1 if masked
   uint64_t full[Fmt<FMT>::kStages];
@@ -154,61 +152,50 @@ __device__ __forceinline__ uint32_t bf16pair_to_f16x2(uint32_t two) {
 }
 
 // Cluster merge: the splits of one (request, head group) are the CTAs of a
-// cluster.  Each has written its normalised partial O and base-2 LSE to the
-// workspace (through L2: distributed shared memory has a fraction of L2's
+// cluster.  Each has written its normalised partial O (f16) and base-2 LSE to
+// the workspace (through L2: distributed shared memory has a fraction of L2's
 // bandwidth per SM); after the cluster barrier (release/acquire at cluster
-// scope) CTA r combines the float4 units r*128 + t + k*S*128 of the 16 x 512
+// scope) CTA r combines the 8-value units r*128 + t + k*S*128 of the 16 x 512
 // output tile from every split: LSE = log2 sum_r 2^lse_r and
 // out = sum_r 2^(lse_r - max) O_r / sum_r 2^(lse_r - max).
-template <typename SmemT>
-__device__ __forceinline__ void cluster_merge(const DecodeArgs& args, SmemT& sm, int v, int hg, int sp) {
+__device__ __forceinline__ void cluster_merge(const DecodeArgs& args, int v, int hg, int sp) {
   cluster_sync_all();
   const int S = args.splits;
   const int64_t bh_base = static_cast<int64_t>(v) * args.num_heads + hg * kHeadsPerCta;
-  // split weights per head: thread t < 16 S reads the LSE of head t / S from
-  // split t % S, then thread h < 16 turns head h's into weights
-  if (static_cast<int>(threadIdx.x) < kHeadsPerCta * S) {
-    const int h = threadIdx.x / S, r = threadIdx.x % S;
-    sm.mw[h][r] = __ldcg(args.part_lse + (bh_base + h) * S + r);
-  }
-  named_bar_sync(1, kThreads);
-  if (threadIdx.x < kHeadsPerCta) {
-    const int h = threadIdx.x;
-    float mx = -INFINITY;
-    for (int r = 0; r < S; ++r) mx = fmaxf(mx, sm.mw[h][r]);
-    float wsum = 0.f;
-    for (int r = 0; r < S; ++r) {
-      const float ws = mx == -INFINITY ? 0.f : ex2(sm.mw[h][r] - mx);  // 0 for an empty split
-      sm.mw[h][r] = ws;
-      wsum += ws;
-    }
-    sm.minv[h] = wsum > 0.f ? 1.f / wsum : 0.f;
-    if (args.lse != nullptr && h % S == sp) args.lse[bh_base + h] = wsum > 0.f ? (mx + lg2(wsum)) * kLn2 : -INFINITY;
-  }
-  named_bar_sync(1, kThreads);
-  // unit u = (head u / 64, dims 8 (u % 64) .. + 8) of the 16 x 512 tile
+  // unit u = (head u / 64, dims 8 (u % 64) .. + 8) of the 16 x 512 tile; a
+  // thread loads the LSEs and partials of two units before using any (one
+  // L2 round trip) and forms the split weights itself
   constexpr int kPerHead = kLatent / 8;
   constexpr int kUnits = kHeadsPerCta * kPerHead;
   const uint4* part = reinterpret_cast<const uint4*>(args.part_o);
   for (int u0 = sp * kThreads + static_cast<int>(threadIdx.x); u0 < kUnits; u0 += 2 * S * kThreads) {
     uint4 pv[2][kMaxClusterSplits];
+    float ls[2][kMaxClusterSplits];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const int u = u0 + i * S * kThreads;
       const int64_t row = (bh_base + u / kPerHead) * S;
 #pragma unroll
-      for (int r = 0; r < kMaxClusterSplits; ++r)
-        pv[i][r] = (u < kUnits && r < S) ? __ldcg(part + (row + r) * kPerHead + u % kPerHead) : make_uint4(0, 0, 0, 0);
+      for (int r = 0; r < kMaxClusterSplits; ++r) {
+        const bool in = u < kUnits && r < S;
+        ls[i][r] = in ? __ldcg(args.part_lse + row + r) : -INFINITY;
+        pv[i][r] = in ? __ldcg(part + (row + r) * kPerHead + u % kPerHead) : make_uint4(0, 0, 0, 0);
+      }
     }
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const int u = u0 + i * S * kThreads;
       if (u < kUnits) {
         const int h = u / kPerHead;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int r = 0; r < kMaxClusterSplits; ++r) mx = fmaxf(mx, ls[i][r]);
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        float wsum = 0.f;
 #pragma unroll
         for (int r = 0; r < kMaxClusterSplits; ++r) {
-          const float ws = r < S ? sm.mw[h][r] : 0.f;
+          const float ws = mx == -INFINITY ? 0.f : ex2(ls[i][r] - mx);  // 0 for an empty split
+          wsum += ws;
           const uint32_t wd[4] = {pv[i][r].x, pv[i][r].y, pv[i][r].z, pv[i][r].w};
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -217,7 +204,7 @@ __device__ __forceinline__ void cluster_merge(const DecodeArgs& args, SmemT& sm,
             acc[2 * k + 1] += ws * f.y;
           }
         }
-        const float inv = sm.minv[h];
+        const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
         uint32_t ob[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -226,6 +213,8 @@ __device__ __forceinline__ void cluster_merge(const DecodeArgs& args, SmemT& sm,
         }
         *reinterpret_cast<uint4*>(args.out + (bh_base + h) * kLatent + 8 * (u % kPerHead)) =
             make_uint4(ob[0], ob[1], ob[2], ob[3]);
+        if (args.lse != nullptr && u % kPerHead == 0)
+          args.lse[bh_base + h] = wsum > 0.f ? (mx + lg2(wsum)) * kLn2 : -INFINITY;
       }
     }
   }
@@ -657,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       args.part_lse[bh0 * args.splits + sp] = lse2_0;
       args.part_lse[bh1 * args.splits + sp] = lse2_1;
     }
-    if (args.cluster_merge) cluster_merge(args, sm, v, hg, sp);
+    if (args.cluster_merge) cluster_merge(args, v, hg, sp);
   }
 }
 
