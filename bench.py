@@ -310,6 +310,10 @@ def main():
     layers = []
     for li in range(L):
         wl = W.tp4_rank_decode(dev, seed=1000 * rank + li, ctx=args.ctx)
+        if layers:
+            # a paged cache keeps one block table per request for every layer
+            # (each layer has its own pool, addressed by the same block ids)
+            wl.block_table, wl.num_blocks = layers[0].block_table, layers[0].num_blocks
         W.fill_pool(wl, 0, qa)
         W.fill_pool(wl, 1, qa)
         wl.out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=dev)
@@ -483,7 +487,8 @@ def main():
         "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": {"workload": f"TP4 rank decode: 32 requests x 16 heads, {args.ctx:,}-token contexts, top-2048 "
                                "(70% prefix + 30% last 6,000), NVFP4 352-byte rows, block 64",
-                   "layers_per_step": L, "l2": f"inputs larger than L2: {L} distinct layer caches, "
+                   "layers_per_step": L, "block_table": "one per request, shared by the layers",
+                   "l2": f"inputs larger than L2: {L} distinct layer caches, "
                                               f"{L * layer_bytes4 / 1e6:.0f} MB read per step vs "
                                               f"{l2 / 1e6:.0f} MB L2",
                    "global_batch": B * world, "seq_len": args.ctx, "parallelism": f"replicas x{world}"},

@@ -133,10 +133,13 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 3) indexer_scores_kernel(const
     for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      uint32_t A0[4] = {e4m3x2_to_f16x2(v0[q].x), e4m3x2_to_f16x2(v1[q].x), e4m3x2_to_f16x2(v0[q].x >> 16),
-                        e4m3x2_to_f16x2(v1[q].x >> 16)};
-      uint32_t A1[4] = {e4m3x2_to_f16x2(v0[q].y), e4m3x2_to_f16x2(v1[q].y), e4m3x2_to_f16x2(v0[q].y >> 16),
-                        e4m3x2_to_f16x2(v1[q].y >> 16)};
+      uint32_t x0[2], x1[2], y0[2], y1[2];
+      e4m3x4_to_f16x2x2(v0[q].x, x0);
+      e4m3x4_to_f16x2x2(v1[q].x, x1);
+      e4m3x4_to_f16x2x2(v0[q].y, y0);
+      e4m3x4_to_f16x2x2(v1[q].y, y1);
+      uint32_t A0[4] = {x0[0], x1[0], x0[1], x1[1]};
+      uint32_t A1[4] = {y0[0], y1[0], y0[1], y1[1]};
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
         mma_f16(acc[n], A0, bq[2 * q][n][0], bq[2 * q][n][1]);
@@ -272,10 +275,13 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 3)
       const int off = (((2 * q + (c >> 1)) ^ g) << 4) + 8 * (c & 1);
       const uint2 v0 = *reinterpret_cast<const uint2*>(row0 + off);
       const uint2 v1 = *reinterpret_cast<const uint2*>(row1 + off);
-      uint32_t A0[4] = {e4m3x2_to_f16x2(v0.x), e4m3x2_to_f16x2(v1.x), e4m3x2_to_f16x2(v0.x >> 16),
-                        e4m3x2_to_f16x2(v1.x >> 16)};
-      uint32_t A1[4] = {e4m3x2_to_f16x2(v0.y), e4m3x2_to_f16x2(v1.y), e4m3x2_to_f16x2(v0.y >> 16),
-                        e4m3x2_to_f16x2(v1.y >> 16)};
+      uint32_t x0[2], x1[2], y0[2], y1[2];
+      e4m3x4_to_f16x2x2(v0.x, x0);
+      e4m3x4_to_f16x2x2(v1.x, x1);
+      e4m3x4_to_f16x2x2(v0.y, y0);
+      e4m3x4_to_f16x2x2(v1.y, y1);
+      uint32_t A0[4] = {x0[0], x1[0], x0[1], x1[1]};
+      uint32_t A1[4] = {y0[0], y1[0], y0[1], y1[1]};
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
         mma_f16(acc[n], A0, bq[2 * q][n][0], bq[2 * q][n][1]);

@@ -38,6 +38,28 @@ __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
   asm("{ .reg .b8 b; cvt.u8.u32 b, %1; cvt.rn.f16x2.e2m1x2 %0, b; }" : "=r"(d) : "r"(byte));
   return d;
 }
+// Eight e2m1 codes (one 32-bit word, element 2i in the low nibble of byte i)
+// to four f16x2 (byte i -> d[i]); the word is split into its bytes by a
+// register unpack, not by shifts.
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&d)[4]) {
+  asm("{ .reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3; }"
+      : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+      : "r"(w));
+}
+// Four e4m3 bytes to two f16x2 (low half-word -> d[0]).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t (&d)[2]) {
+  asm("{ .reg .b16 h0, h1;\n\t"
+      "mov.b32 {h0, h1}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, h0;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h1; }"
+      : "=r"(d[0]), "=r"(d[1])
+      : "r"(w));
+}
 // Two e4m3 bytes (low byte -> low half) to two exact f16 values.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
   uint32_t d;

@@ -347,10 +347,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       cp_async_arrive(&sm.full[slot]);
     }
   };
-  // Only two stages up front: the copies of every CTA start together, and a
-  // deeper initial burst would only delay the first stage behind the others.
-  // The rest of the ring is filled at the following stage boundaries.
-  constexpr int kInitialStages = 2;
+  // One stage up front: the copies of every CTA start together, and any
+  // deeper initial burst only delays the first stage behind the others (all
+  // of them compete for HBM at once).  The next stages are issued at the
+  // following stage boundaries.
+  constexpr int kInitialStages = 1;
   int next_fill = 0;
   for (; next_fill < min(n_stages, kInitialStages); ++next_fill) fill_stage(next_fill);
 
@@ -387,9 +388,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int slot = it % kStages;
     const uint32_t round = it / kStages;
     if constexpr (TMA) {
-      // Every warp finished reading stage it - 1's slot before the first
-      // barrier of that stage, so stages up to it - 1 + kStages may be issued.
-      for (; next_fill < n_stages && next_fill <= it - 1 + kStages; ++next_fill) fill_stage(next_fill);
+      // One stage ahead: stage it + 1 is issued as stage it begins (its slot
+      // held stage it - 1, which every warp finished reading before that
+      // stage's first barrier).  Prefetching deeper measured slower: the
+      // extra bytes in flight delay the stage being waited on.
+      for (; next_fill < n_stages && next_fill <= min(it + 1, it - 1 + kStages); ++next_fill) fill_stage(next_fill);
     }
     const bool ok = mbar_wait_bounded(&sm.full[slot], round & 1u, args.fault_word, kFaultDecodeWait);
     if (!__all_sync(0xFFFFFFFFu, ok) && lane == 0) sm.abort_flag = 1;  // all warps leave after the next barrier
@@ -418,14 +421,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t w1 = *reinterpret_cast<const uint32_t*>(row1 + off);
           const uint32_t s0 = __byte_perm(q < 2 ? s0_01 : s0_23, 0, (q & 1) ? 0x3232 : 0x1010);
           const uint32_t s1 = __byte_perm(q < 2 ? s1_01 : s1_23, 0, (q & 1) ? 0x3232 : 0x1010);
-          a[mt][2 * q][0] = hmul2(e2m1x2_to_f16x2(w0 & 0xFFu), s0);
-          a[mt][2 * q][1] = hmul2(e2m1x2_to_f16x2(w1 & 0xFFu), s1);
-          a[mt][2 * q][2] = hmul2(e2m1x2_to_f16x2((w0 >> 8) & 0xFFu), s0);
-          a[mt][2 * q][3] = hmul2(e2m1x2_to_f16x2((w1 >> 8) & 0xFFu), s1);
-          a[mt][2 * q + 1][0] = hmul2(e2m1x2_to_f16x2((w0 >> 16) & 0xFFu), s0);
-          a[mt][2 * q + 1][1] = hmul2(e2m1x2_to_f16x2((w1 >> 16) & 0xFFu), s1);
-          a[mt][2 * q + 1][2] = hmul2(e2m1x2_to_f16x2(w0 >> 24), s0);
-          a[mt][2 * q + 1][3] = hmul2(e2m1x2_to_f16x2(w1 >> 24), s1);
+          uint32_t d0[4], d1[4];
+          e2m1x8_to_f16x2x4(w0, d0);
+          e2m1x8_to_f16x2x4(w1, d1);
+          a[mt][2 * q][0] = hmul2(d0[0], s0);
+          a[mt][2 * q][1] = hmul2(d1[0], s1);
+          a[mt][2 * q][2] = hmul2(d0[1], s0);
+          a[mt][2 * q][3] = hmul2(d1[1], s1);
+          a[mt][2 * q + 1][0] = hmul2(d0[2], s0);
+          a[mt][2 * q + 1][1] = hmul2(d1[2], s1);
+          a[mt][2 * q + 1][2] = hmul2(d0[3], s0);
+          a[mt][2 * q + 1][3] = hmul2(d1[3], s1);
         }
       } else {
 #pragma unroll
@@ -433,23 +439,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int off = 128 * w + 32 * q + 8 * c;
           const uint2 v0 = *reinterpret_cast<const uint2*>(row0 + off);
           const uint2 v1 = *reinterpret_cast<const uint2*>(row1 + off);
-          a[mt][2 * q][0] = e4m3x2_to_f16x2(v0.x);
-          a[mt][2 * q][1] = e4m3x2_to_f16x2(v1.x);
-          a[mt][2 * q][2] = e4m3x2_to_f16x2(v0.x >> 16);
-          a[mt][2 * q][3] = e4m3x2_to_f16x2(v1.x >> 16);
-          a[mt][2 * q + 1][0] = e4m3x2_to_f16x2(v0.y);
-          a[mt][2 * q + 1][1] = e4m3x2_to_f16x2(v1.y);
-          a[mt][2 * q + 1][2] = e4m3x2_to_f16x2(v0.y >> 16);
-          a[mt][2 * q + 1][3] = e4m3x2_to_f16x2(v1.y >> 16);
+          uint32_t lo0[2], lo1[2], hi0[2], hi1[2];
+          e4m3x4_to_f16x2x2(v0.x, lo0);
+          e4m3x4_to_f16x2x2(v1.x, lo1);
+          e4m3x4_to_f16x2x2(v0.y, hi0);
+          e4m3x4_to_f16x2x2(v1.y, hi1);
+          a[mt][2 * q][0] = lo0[0];
+          a[mt][2 * q][1] = lo1[0];
+          a[mt][2 * q][2] = lo0[1];
+          a[mt][2 * q][3] = lo1[1];
+          a[mt][2 * q + 1][0] = hi0[0];
+          a[mt][2 * q + 1][1] = hi1[0];
+          a[mt][2 * q + 1][2] = hi0[1];
+          a[mt][2 * q + 1][3] = hi1[1];
         }
       }
       const int roff = F::kRopeOff + 16 * w + 4 * c;
       const uint32_t x0 = *reinterpret_cast<const uint32_t*>(row0 + roff);
       const uint32_t x1 = *reinterpret_cast<const uint32_t*>(row1 + roff);
-      a[mt][8][0] = e4m3x2_to_f16x2(x0);
-      a[mt][8][1] = e4m3x2_to_f16x2(x1);
-      a[mt][8][2] = e4m3x2_to_f16x2(x0 >> 16);
-      a[mt][8][3] = e4m3x2_to_f16x2(x1 >> 16);
+      {
+        uint32_t r0[2], r1[2];
+        e4m3x4_to_f16x2x2(x0, r0);
+        e4m3x4_to_f16x2x2(x1, r1);
+        a[mt][8][0] = r0[0];
+        a[mt][8][1] = r1[0];
+        a[mt][8][2] = r0[1];
+        a[mt][8][3] = r1[1];
+      }
     }
 
     // ---- partial scores over this warp's 144 dims: S^T [32 tokens x 16 heads]
