@@ -67,7 +67,7 @@ constexpr int kRedPitch = 24;  // floats per token row of the partial-score exch
 constexpr int kPPitch = 40;    // halfs per head row of P (80 bytes: ldmatrix conflict-free)
 constexpr int kKSteps = 9;     // k-steps of 16 dims per consumer warp (128 latent + 16 rope)
 // Splits of one (request, head group) up to this many form a thread-block
-// cluster and merge their partials through distributed shared memory.
+// cluster and merge their partials inside the decode kernel.
 constexpr int kMaxClusterSplits = 8;
 // Lazy softmax maximum: scores are exponentiated against a reference maximum
 // that is raised only when a score exceeds it by more than kLazy (base 2), so
@@ -786,10 +786,21 @@ DecodePlan plan_sparse_decode(int batch, int num_heads, int topk) {
   DecodePlan p{1, 0, false, 0};
   const int groups = batch * (num_heads / kHeadsPerCta);
   const int slots = 2 * device_sm_count();  // two CTAs per SM fit (registers, shared memory)
-  int splits = groups > 0 ? slots / groups : 1;
   const int max_splits = (topk + kStageRows - 1) / kStageRows;
   const int min_splits = (topk + kMaxRows - 1) / kMaxRows;  // a slice fits the CTA's row tables
-  splits = splits < min_splits ? min_splits : (splits > max_splits ? max_splits : splits);
+  // Modelled time: waves of CTAs x (32-row stages per CTA + ~2 stages of
+  // start-up latency per CTA); the fewest splits among the cheapest.
+  int splits = min_splits;
+  long long best = -1;
+  for (int s = min_splits; s <= max_splits && groups > 0; ++s) {
+    const long long waves = (static_cast<long long>(groups) * s + slots - 1) / slots;
+    const int st = ((topk + s - 1) / s + kStageRows - 1) / kStageRows;
+    const long long cost = waves * (st + 2);
+    if (best < 0 || cost < best) {
+      best = cost;
+      splits = s;
+    }
+  }
   // The critical path is the number of 32-row stages per CTA: keep it, but
   // with as few splits as give it (fewer, fuller CTAs and partials to merge).
   const int stages = ((topk + splits - 1) / splits + kStageRows - 1) / kStageRows;
