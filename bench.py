@@ -56,6 +56,8 @@ def parse():
     p.add_argument("--only-extras", action="store_true", help="time only the sub-benchmarks (profiling)")
     p.add_argument("--draft-tokens", type=int, default=4, help="query tokens per request in the draft-token timing")
     p.add_argument("--no-dep", action="store_true", help="skip the 128 x 64-head (DEP rank) decode timing")
+    p.add_argument("--dep-tokens", type=int, default=24_000_000,
+                   help="cached tokens of the DEP rank in total (a smaller pool, same 128 x 2,048 selected rows)")
     return p.parse_args()
 
 
@@ -619,7 +621,7 @@ def dep_measurement(m, W, dev, stream, args, hbm):
     events after an L2 flush (the selected rows of one layer fit in L2)."""
     import torch
     _, tf_burst, _, _ = peaks()
-    wl = W.dep_rank_decode(dev)
+    wl = W.dep_rank_decode(dev, cap=args.dep_tokens)
 
     def qa(lat, rope, slots, pool, nb, stride, fmt):
         m.mla_kv_quantize_append(lat, rope, slots, pool, nb, 64, stride, fmt)

@@ -220,13 +220,15 @@ def dep_rank_context_lens(seed: int = 0, batch: int = 128, lo: int = 8192, hi: i
     return [int(x) for x in ctx]
 
 
-def dep_rank_decode(device, seed: int = 0, batch: int = 128, heads: int = 64, topk: int = 2048) -> DecodeWorkload:
+def dep_rank_decode(device, seed: int = 0, batch: int = 128, heads: int = 64, topk: int = 2048,
+                    cap: int = 24_000_000) -> DecodeWorkload:
     """All heads per rank (DEP-style): 128 requests x 64 heads, contexts
-    log-uniform in [8,192, 1,048,576] capped at 24M tokens in total, top-2048
-    uniform without replacement over each context."""
-    ctx = dep_rank_context_lens(seed, batch)
+    log-uniform in [8,192, 1,048,576] capped at `cap` tokens in total (24M),
+    top-2048 uniform without replacement over each context."""
+    ctx = dep_rank_context_lens(seed, batch, cap=cap)
+    seed_parts = ("dep", seed, batch, heads, topk) if cap == 24_000_000 else ("dep", seed, batch, heads, topk, cap)
     return _decode_workload(f"DEP rank: {batch} requests x {heads} heads, contexts 8K-1M (sum {sum(ctx):,}), top-{topk}",
-                            ("dep", seed, batch, heads, topk), batch, heads, topk, ctx, device, 0.0,
+                            seed_parts, batch, heads, topk, ctx, device, 0.0,
                             lambda b, c, g: distinct_uniform(min(topk, c), 0, c, g, device))
 
 
