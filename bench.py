@@ -76,6 +76,7 @@ def peaks():
 # selected rows; profiles/sparse_decode_nvfp4_tp4_rank.md), and a digest of
 # the kernel source it was taken on: once the source differs, the figure no
 # longer describes the kernel and is reported as null.
+E2E_CHUNKS = 4  # copy chunks per step of the end-to-end pass
 DECODE_NVFP4_TRAFFIC = {"bytes": 29_490_688 + 6_912, "source_digest": "43d303137e2341e0"}
 KERNEL_SOURCES = ("sparse_mla_decode_kv_gb300/csrc/sparse_decode.cu", "sparse_mla_decode_kv_gb300/csrc/mla_device.cuh")
 
@@ -410,11 +411,12 @@ def main():
     roof_t8 = max(layer_bytes8 / (hbm * 1e9), fl / (tf_burst * 1e12))
 
     # ---- end to end through the C ABI with host buffers (pinned): per step,
-    # one H2D copy of every layer's packed inputs (q_nope, q_rope, top-k list,
-    # context lengths), the L decodes on views of that device buffer, and one
-    # D2H copy of every layer's packed outputs (out, lse); the copies and the
-    # decodes are captured together in one CUDA graph.  (Copying per layer
-    # cost ~14 us of copy-engine time per layer, more than the decode.)
+    # every layer's packed inputs (q_nope, q_rope, top-k list, context
+    # lengths) are copied H2D, the L decodes run on views of that device
+    # buffer, and every layer's packed outputs (out, lse) are copied D2H; the
+    # copies go in a few large chunks on a second stream, overlapping the
+    # decodes, all captured in one CUDA graph.  (Copying per layer cost ~14 us
+    # of copy-engine time per layer, more than the decode.)
     names = ("q_nope", "q_rope", "topk_idx", "context_lens")
 
     def layout(tensors):
@@ -447,14 +449,38 @@ def main():
     h2d = in_bytes * L
     d2h = out_bytes * L
 
+    # The step's layers in E2E_CHUNKS chunks: a second stream copies chunk
+    # c + 1's inputs and chunk c - 1's outputs while chunk c decodes.
+    n_chunks = min(E2E_CHUNKS, L)
+    bounds = [(L * c // n_chunks, L * (c + 1) // n_chunks) for c in range(n_chunks)]
+    copy_stream = torch.cuda.Stream(device=dev)
+
     def e2e_step():
-        d_in_buf.copy_(host_in, non_blocking=True)
-        for li, wl in enumerate(layers):
-            x = d_in[li]
-            m.mla_sparse_decode(x["q_nope"], x["q_rope"], wl.pools[0], wl.strides[0], wl.num_blocks,
-                                wl.block_table, x["context_lens"], x["topk_idx"], wl.softmax_scale,
-                                out=d_out[li][0], lse=d_out[li][1], workspace=workspace, stream=stream)
-        h_out_buf.copy_(d_out_buf, non_blocking=True)
+        copy_stream.wait_stream(stream)
+        h2d_done = []
+        with torch.cuda.stream(copy_stream):
+            for lo, hi in bounds:
+                d_in_buf[lo * in_bytes:hi * in_bytes].copy_(host_in[lo * in_bytes:hi * in_bytes], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(copy_stream)
+                h2d_done.append(ev)
+        dec_done = []
+        for (lo, hi), ev in zip(bounds, h2d_done):
+            stream.wait_event(ev)
+            for li in range(lo, hi):
+                wl, x = layers[li], d_in[li]
+                m.mla_sparse_decode(x["q_nope"], x["q_rope"], wl.pools[0], wl.strides[0], wl.num_blocks,
+                                    wl.block_table, x["context_lens"], x["topk_idx"], wl.softmax_scale,
+                                    out=d_out[li][0], lse=d_out[li][1], workspace=workspace, stream=stream)
+            ev2 = torch.cuda.Event()
+            ev2.record(stream)
+            dec_done.append(ev2)
+        with torch.cuda.stream(copy_stream):
+            for (lo, hi), ev2 in zip(bounds, dec_done):
+                copy_stream.wait_event(ev2)
+                h_out_buf[lo * out_bytes:hi * out_bytes].copy_(d_out_buf[lo * out_bytes:hi * out_bytes],
+                                                               non_blocking=True)
+        stream.wait_stream(copy_stream)
 
     g_e2e = capture(e2e_step)
     with torch.cuda.stream(stream):
