@@ -14,15 +14,15 @@
 //  * One CTA = one request x 16 heads x one contiguous slice of its top-k
 //    list; four warps, all of which load, unpack and compute.  At entry the
 //    CTA resolves every row of its slice (top-k index, then block table) in
-//    batches of independent loads and keeps the byte offsets in shared
+//    batches of independent loads and keeps the row positions in shared
 //    memory; rows that are masked (-1, past the context, logical block past
-//    the table, block id outside the pool) get offset -1.
+//    the table, block id outside the pool) get -1.
 //  * Rows travel in stages of 32 through a ring of shared-memory slots (4
-//    for NVFP4, 3 for FP8).  Every thread issues 16-byte cp.async copies for
-//    its share of a stage (masked rows are zero-filled, nothing is read) and
-//    then arrives on the slot's mbarrier through cp.async.mbarrier.arrive, so
-//    the barrier completes when all copies of the stage have landed.  Two
-//    stages are issued up front and up to two more at each stage boundary.
+//    for NVFP4, 3 for FP8).  When the pool's block stride is a whole number
+//    of rows, the pool is a 2-D tensor of rows to TMA and each warp gathers
+//    its 8 rows of a stage with two 4-row tile::gather4 copies (a masked row
+//    is coordinate -1 and reads zeros), one stage ahead.  Other pools use
+//    16-byte cp.async from every thread, arriving on the slot's mbarrier.
 //  * Warp w owns latent dims [128w, 128w+128) and rope dims [16w, 16w+16):
 //    it unpacks only those bytes of both 16-row m-tiles, straight into
 //    mma.sync A fragments (cvt e2m1x2 / e4m3x2 -> f16x2, times the group's
@@ -42,10 +42,10 @@
 //    the query fragments use the same permutation and the output is written
 //    back in natural order.
 //  * When a request's list is split over several CTAs, each writes its
-//    normalised partial output and base-2 LSE to the workspace and a small
-//    merge kernel, launched as a programmatic dependent of the decode grid,
-//    combines them (the pages merge in-cluster through distributed shared
-//    memory; this build uses a second launch).
+//    normalised partial output (f16) and base-2 LSE to the workspace.  Up to
+//    8 splits form a thread-block cluster and merge inside this kernel after
+//    a cluster barrier, as the pages' kernel merges in-cluster; more splits
+//    are merged by a small kernel launched as a programmatic dependent.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
