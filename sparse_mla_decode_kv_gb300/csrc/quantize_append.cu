@@ -131,9 +131,9 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     for (int u = 0; u < kUnroll; ++u) {
       const int64_t n = 2 * (pair0 + u * warp_stride) + half;
       slots[u] = n < n_tokens ? __ldg(slot_mapping + n) : -1;
-      vs[u] = make_uint4(0, 0, 0, 0);
-      if (slots[u] >= 0 && slots[u] / kBlock < num_blocks)
-        vs[u] = __ldg(reinterpret_cast<const uint4*>(keys + n * kIdxDim) + l16);
+      // the key's load does not wait for its slot (a skipped token's key is
+      // read and dropped): one memory round trip per batch, not two
+      vs[u] = n < n_tokens ? __ldg(reinterpret_cast<const uint4*>(keys + n * kIdxDim) + l16) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
