@@ -111,68 +111,71 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 // Indexer keys ("GLM-5.3 PCP/DCP long-context on H200", section 3: 128 FP8
 // values plus a 4-byte scale per token): s = amax / 448 and codes
 // e4m3(k / s), both divisions IEEE single precision; a zero key stores s = 0
-// and zero codes.  Half a warp per token: lane l of the half owns values
-// [8l, 8l+8) (one 16-byte load, one 8-byte store); the amax is a 16-lane
-// shuffle reduction.  Block layout: 64 x 128 code bytes, then 64 floats.
+// and zero codes.  A quarter warp per token: lane l of the quarter owns
+// values [16l, 16l+16) (two 16-byte loads, one 16-byte store), so the
+// per-token scale and reciprocal are shared by 16 values per lane; the amax
+// is an 8-lane shuffle reduction.  Block layout: 64 x 128 code bytes, then
+// 64 floats.
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     index_key_append_kernel(const uint16_t* __restrict__ keys, const int64_t* __restrict__ slot_mapping,
                             int64_t n_tokens, uint8_t* __restrict__ pool, int64_t num_blocks,
                             int64_t block_stride) {
-  constexpr int kUnroll = 4;  // pairs of tokens per warp per iteration: all their loads are issued first
+  constexpr int kUnroll = 2;  // groups of 4 tokens per warp per iteration: all their loads are issued first
   const int lane = threadIdx.x & 31;
-  const int half = lane >> 4;
-  const int l16 = lane & 15;
+  const int quarter = lane >> 3;
+  const int l8 = lane & 7;
   const int64_t warp_global = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
   const int64_t warp_stride = static_cast<int64_t>(gridDim.x) * kWarpsPerBlock;
-  for (int64_t pair0 = warp_global; 2 * pair0 < n_tokens; pair0 += kUnroll * warp_stride) {
+  for (int64_t quad0 = warp_global; 4 * quad0 < n_tokens; quad0 += kUnroll * warp_stride) {
     int64_t slots[kUnroll];
-    uint4 vs[kUnroll];
+    uint4 va[kUnroll], vb[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const int64_t n = 2 * (pair0 + u * warp_stride) + half;
-      slots[u] = n < n_tokens ? __ldg(slot_mapping + n) : -1;
+      const int64_t n = 4 * (quad0 + u * warp_stride) + quarter;
+      const bool in = n < n_tokens;
+      slots[u] = in ? __ldg(slot_mapping + n) : -1;
       // the key's load does not wait for its slot (a skipped token's key is
       // read and dropped): one memory round trip per batch, not two
-      vs[u] = n < n_tokens ? __ldg(reinterpret_cast<const uint4*>(keys + n * kIdxDim) + l16) : make_uint4(0, 0, 0, 0);
+      const uint4* src = reinterpret_cast<const uint4*>(keys + n * kIdxDim) + 2 * l8;
+      va[u] = in ? __ldg(src) : make_uint4(0, 0, 0, 0);
+      vb[u] = in ? __ldg(src + 1) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      if (2 * (pair0 + u * warp_stride) >= n_tokens) break;  // warp-uniform
+      if (4 * (quad0 + u * warp_stride) >= n_tokens) break;  // warp-uniform
       const int64_t slot = slots[u];
       const bool ok = slot >= 0 && slot / kBlock < num_blocks;
-      const uint32_t w[4] = {vs[u].x, vs[u].y, vs[u].z, vs[u].w};
-      float x[8];
+      const uint32_t w[8] = {va[u].x, va[u].y, va[u].z, va[u].w, vb[u].x, vb[u].y, vb[u].z, vb[u].w};
+      float x[16];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < 8; ++i) {
         x[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
         x[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
       }
       float amax = 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
 #pragma unroll
-      for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+      for (int off = 4; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
       if (!ok) continue;
       const float s = amax == 0.f ? 0.f : __fdiv_rn(amax, 448.0f);
-      uint32_t lo = 0, hi = 0;
+      uint32_t q[4] = {0u, 0u, 0u, 0u};  // 16 codes, value 4k + j in byte j of q[k]
       if (amax != 0.f && s >= 1.17549435e-38f) {  // normal scale: reciprocal and one correction
         const float r = __frcp_rn(s);
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          lo |= f32x2_to_e4m3x2(div_rn(x[2 * i + 1], s, r), div_rn(x[2 * i], s, r)) << (16 * i);
-          hi |= f32x2_to_e4m3x2(div_rn(x[4 + 2 * i + 1], s, r), div_rn(x[4 + 2 * i], s, r)) << (16 * i);
-        }
+        for (int k = 0; k < 4; ++k)
+          q[k] = f32x2_to_e4m3x2(div_rn(x[4 * k + 1], s, r), div_rn(x[4 * k], s, r)) |
+                 (f32x2_to_e4m3x2(div_rn(x[4 * k + 3], s, r), div_rn(x[4 * k + 2], s, r)) << 16);
       } else if (amax != 0.f) {  // subnormal scale (1/s overflows): plain IEEE division
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          lo |= f32x2_to_e4m3x2(__fdiv_rn(x[2 * i + 1], s), __fdiv_rn(x[2 * i], s)) << (16 * i);
-          hi |= f32x2_to_e4m3x2(__fdiv_rn(x[4 + 2 * i + 1], s), __fdiv_rn(x[4 + 2 * i], s)) << (16 * i);
-        }
+        for (int k = 0; k < 4; ++k)
+          q[k] = f32x2_to_e4m3x2(__fdiv_rn(x[4 * k + 1], s), __fdiv_rn(x[4 * k], s)) |
+                 (f32x2_to_e4m3x2(__fdiv_rn(x[4 * k + 3], s), __fdiv_rn(x[4 * k + 2], s)) << 16);
       }
       uint8_t* blk = pool + (slot / kBlock) * block_stride;
       const int64_t o = slot % kBlock;
-      *reinterpret_cast<uint2*>(blk + o * kIdxDim + 8 * l16) = make_uint2(lo, hi);
-      if (l16 == 0) *reinterpret_cast<float*>(blk + static_cast<int64_t>(kBlock) * kIdxDim + 4 * o) = s;
+      *reinterpret_cast<uint4*>(blk + o * kIdxDim + 16 * l8) = make_uint4(q[0], q[1], q[2], q[3]);
+      if (l8 == 0) *reinterpret_cast<float*>(blk + static_cast<int64_t>(kBlock) * kIdxDim + 4 * o) = s;
     }
   }
 }
@@ -182,8 +185,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 cudaError_t launch_index_key_append(const uint16_t* keys, const int64_t* slot_mapping, int64_t n_tokens, void* pool,
                                     int64_t num_blocks, int64_t block_stride, cudaStream_t stream) {
   if (n_tokens <= 0) return cudaSuccess;
-  const int64_t pairs = (n_tokens + 1) / 2;
-  int64_t want = (pairs + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  const int64_t quads = (n_tokens + 3) / 4;
+  int64_t want = (quads + kWarpsPerBlock - 1) / kWarpsPerBlock;
   const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
   const int grid = static_cast<int>(want < cap ? want : cap);
   index_key_append_kernel<<<grid, kWarpsPerBlock * 32, 0, stream>>>(keys, slot_mapping, n_tokens,
