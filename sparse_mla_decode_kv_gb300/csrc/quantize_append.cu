@@ -111,70 +111,72 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 // Indexer keys ("GLM-5.3 PCP/DCP long-context on H200", section 3: 128 FP8
 // values plus a 4-byte scale per token): s = amax / 448 and codes
 // e4m3(k / s), both divisions IEEE single precision; a zero key stores s = 0
-// and zero codes.  A quarter warp per token: lane l of the quarter owns
-// values [16l, 16l+16) (two 16-byte loads, one 16-byte store), so the
-// per-token scale and reciprocal are shared by 16 values per lane; the amax
-// is an 8-lane shuffle reduction.  Block layout: 64 x 128 code bytes, then
-// 64 floats.
+// and zero codes.  Four lanes per token: lane l of the four owns values
+// [32l, 32l+32) (four 16-byte loads, two 16-byte stores), so the per-token
+// scale and reciprocal are shared by 32 values per lane; the amax is a
+// 4-lane shuffle reduction.  Block layout: 64 x 128 code bytes, then 64
+// floats.
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     index_key_append_kernel(const uint16_t* __restrict__ keys, const int64_t* __restrict__ slot_mapping,
                             int64_t n_tokens, uint8_t* __restrict__ pool, int64_t num_blocks,
                             int64_t block_stride) {
-  constexpr int kUnroll = 2;  // groups of 4 tokens per warp per iteration: all their loads are issued first
+  constexpr int kUnroll = 1;  // groups of 8 tokens per warp per iteration (loads of the group issued first)
   const int lane = threadIdx.x & 31;
-  const int quarter = lane >> 3;
-  const int l8 = lane & 7;
+  const int quarter = lane >> 2;  // token of the group
+  const int l8 = lane & 3;        // lane within the token
   const int64_t warp_global = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
   const int64_t warp_stride = static_cast<int64_t>(gridDim.x) * kWarpsPerBlock;
-  for (int64_t quad0 = warp_global; 4 * quad0 < n_tokens; quad0 += kUnroll * warp_stride) {
+  for (int64_t quad0 = warp_global; 8 * quad0 < n_tokens; quad0 += kUnroll * warp_stride) {
     int64_t slots[kUnroll];
-    uint4 va[kUnroll], vb[kUnroll];
+    uint4 vv[kUnroll][4];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const int64_t n = 4 * (quad0 + u * warp_stride) + quarter;
+      const int64_t n = 8 * (quad0 + u * warp_stride) + quarter;
       const bool in = n < n_tokens;
       slots[u] = in ? __ldg(slot_mapping + n) : -1;
-      // the key's load does not wait for its slot (a skipped token's key is
-      // read and dropped): one memory round trip per batch, not two
-      const uint4* src = reinterpret_cast<const uint4*>(keys + n * kIdxDim) + 2 * l8;
-      va[u] = in ? __ldg(src) : make_uint4(0, 0, 0, 0);
-      vb[u] = in ? __ldg(src + 1) : make_uint4(0, 0, 0, 0);
+      const uint4* src = reinterpret_cast<const uint4*>(keys + n * kIdxDim) + 4 * l8;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) vv[u][k] = in ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      if (4 * (quad0 + u * warp_stride) >= n_tokens) break;  // warp-uniform
+      if (8 * (quad0 + u * warp_stride) >= n_tokens) break;  // warp-uniform
       const int64_t slot = slots[u];
       const bool ok = slot >= 0 && slot / kBlock < num_blocks;
-      const uint32_t w[8] = {va[u].x, va[u].y, va[u].z, va[u].w, vb[u].x, vb[u].y, vb[u].z, vb[u].w};
-      float x[16];
+      float x[32];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        x[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
-        x[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t w[4] = {vv[u][k].x, vv[u][k].y, vv[u][k].z, vv[u][k].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          x[8 * k + 2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
+          x[8 * k + 2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+        }
       }
       float amax = 0.f;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
 #pragma unroll
-      for (int off = 4; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+      for (int off = 2; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
       if (!ok) continue;
       const float s = amax == 0.f ? 0.f : __fdiv_rn(amax, 448.0f);
-      uint32_t q[4] = {0u, 0u, 0u, 0u};  // 16 codes, value 4k + j in byte j of q[k]
+      uint32_t q[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};  // 32 codes, value 4k + j in byte j of q[k]
       if (amax != 0.f && s >= 1.17549435e-38f) {  // normal scale: reciprocal and one correction
         const float r = __frcp_rn(s);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
+        for (int k = 0; k < 8; ++k)
           q[k] = f32x2_to_e4m3x2(div_rn(x[4 * k + 1], s, r), div_rn(x[4 * k], s, r)) |
                  (f32x2_to_e4m3x2(div_rn(x[4 * k + 3], s, r), div_rn(x[4 * k + 2], s, r)) << 16);
       } else if (amax != 0.f) {  // subnormal scale (1/s overflows): plain IEEE division
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
+        for (int k = 0; k < 8; ++k)
           q[k] = f32x2_to_e4m3x2(__fdiv_rn(x[4 * k + 1], s), __fdiv_rn(x[4 * k], s)) |
                  (f32x2_to_e4m3x2(__fdiv_rn(x[4 * k + 3], s), __fdiv_rn(x[4 * k + 2], s)) << 16);
       }
       uint8_t* blk = pool + (slot / kBlock) * block_stride;
       const int64_t o = slot % kBlock;
-      *reinterpret_cast<uint4*>(blk + o * kIdxDim + 16 * l8) = make_uint4(q[0], q[1], q[2], q[3]);
+      *reinterpret_cast<uint4*>(blk + o * kIdxDim + 32 * l8) = make_uint4(q[0], q[1], q[2], q[3]);
+      *reinterpret_cast<uint4*>(blk + o * kIdxDim + 32 * l8 + 16) = make_uint4(q[4], q[5], q[6], q[7]);
       if (l8 == 0) *reinterpret_cast<float*>(blk + static_cast<int64_t>(kBlock) * kIdxDim + 4 * o) = s;
     }
   }
@@ -185,7 +187,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 cudaError_t launch_index_key_append(const uint16_t* keys, const int64_t* slot_mapping, int64_t n_tokens, void* pool,
                                     int64_t num_blocks, int64_t block_stride, cudaStream_t stream) {
   if (n_tokens <= 0) return cudaSuccess;
-  const int64_t quads = (n_tokens + 3) / 4;
+  const int64_t quads = (n_tokens + 7) / 8;
   int64_t want = (quads + kWarpsPerBlock - 1) / kWarpsPerBlock;
   const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
   const int grid = static_cast<int>(want < cap ? want : cap);
