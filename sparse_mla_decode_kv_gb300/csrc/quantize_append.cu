@@ -122,8 +122,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
                             int64_t block_stride) {
   constexpr int kUnroll = 1;  // groups of 8 tokens per warp per iteration (loads of the group issued first)
   const int lane = threadIdx.x & 31;
-  const int quarter = lane >> 2;  // token of the group
-  const int l8 = lane & 3;        // lane within the token
+  const int tok = lane >> 2;  // token of the group
+  const int lt = lane & 3;    // lane within the token
   const int64_t warp_global = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
   const int64_t warp_stride = static_cast<int64_t>(gridDim.x) * kWarpsPerBlock;
   for (int64_t quad0 = warp_global; 8 * quad0 < n_tokens; quad0 += kUnroll * warp_stride) {
@@ -131,10 +131,10 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     uint4 vv[kUnroll][4];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const int64_t n = 8 * (quad0 + u * warp_stride) + quarter;
+      const int64_t n = 8 * (quad0 + u * warp_stride) + tok;
       const bool in = n < n_tokens;
       slots[u] = in ? __ldg(slot_mapping + n) : -1;
-      const uint4* src = reinterpret_cast<const uint4*>(keys + n * kIdxDim) + 4 * l8;
+      const uint4* src = reinterpret_cast<const uint4*>(keys + n * kIdxDim) + 4 * lt;
 #pragma unroll
       for (int k = 0; k < 4; ++k) vv[u][k] = in ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
     }
@@ -175,9 +175,9 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
       }
       uint8_t* blk = pool + (slot / kBlock) * block_stride;
       const int64_t o = slot % kBlock;
-      *reinterpret_cast<uint4*>(blk + o * kIdxDim + 32 * l8) = make_uint4(q[0], q[1], q[2], q[3]);
-      *reinterpret_cast<uint4*>(blk + o * kIdxDim + 32 * l8 + 16) = make_uint4(q[4], q[5], q[6], q[7]);
-      if (l8 == 0) *reinterpret_cast<float*>(blk + static_cast<int64_t>(kBlock) * kIdxDim + 4 * o) = s;
+      *reinterpret_cast<uint4*>(blk + o * kIdxDim + 32 * lt) = make_uint4(q[0], q[1], q[2], q[3]);
+      *reinterpret_cast<uint4*>(blk + o * kIdxDim + 32 * lt + 16) = make_uint4(q[4], q[5], q[6], q[7]);
+      if (lt == 0) *reinterpret_cast<float*>(blk + static_cast<int64_t>(kBlock) * kIdxDim + 4 * o) = s;
     }
   }
 }
