@@ -79,6 +79,7 @@ def small_workload(batch, heads, topk, ctx_lens, seed, device=DEV):
     (2, 16, 2048, [150_000, 2049]),        # full top-k, many splits
     (4, 64, 97, [97, 64, 1, 4096]),        # k not a multiple of 16; ctx < k pads with -1
     (1, 128, 1, [10]),                      # k = 1, eight head groups
+    (2, 128, 700, [3000, 650]),             # two 64-head blocks, ragged stages, ctx < k
     (5, 16, 33, [33, 40, 50, 60, 70]),
 ])
 def test_small_shapes(fmt, batch, heads, topk, ctx_lens):
