@@ -180,6 +180,13 @@ size_t mla_sparse_decode_workspace_size(int batch, int num_heads, int topk);
  * splits, merged by a second kernel.  Output pointers may be NULL.
  * MLA_ERR_INVALID_ARG for batch < 1, num_heads not a positive multiple of
  * 16, or topk < 1.
+ *
+ * The plan describes the 16-head kernel.  An NVFP4 call whose num_heads is a
+ * multiple of 64 and whose pool stride is a whole number of 352-byte rows
+ * runs the tensor-memory kernel instead: one CTA per (request, 64-head
+ * block) and split, min(SMs / blocks, ceil(topk / 128), *splits) splits of
+ * equal length (at least 1), merged by a second kernel when there are
+ * several.  The workspace size covers both.
  */
 mla_status_t mla_sparse_decode_plan(int batch, int num_heads, int topk, int* splits, int* rows_per_split,
                                     int* kernels);

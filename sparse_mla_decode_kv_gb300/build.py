@@ -18,7 +18,7 @@ BUILD = os.path.join(CSRC, "_build")
 LIB = os.path.join(HERE, "libmla_nvfp4.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 SOURCES = ["mla_api.cu", "quantize_append.cu", "sparse_decode.cu", "indexer_topk.cu",
-           "sparse_decode_noalloc.cu", "stage_fp8.cu"]
+           "sparse_decode_noalloc.cu", "stage_fp8.cu", "sparse_decode_tc.cu"]
 HEADERS = ["mla_device.cuh", "mla_internal.h"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

@@ -51,6 +51,34 @@ cudaError_t launch_sparse_decode(int fmt, const uint16_t* q_nope, const uint16_t
                                  int batch, int q_len, int num_heads, int topk, float softmax_scale, uint16_t* out,
                                  float* lse, void* workspace, const DecodePlan& plan, cudaStream_t stream);
 
+// Tensor-memory decode for 64-head blocks of NVFP4 rows in a pool TMA can
+// gather from (sparse_decode_tc.cu).  Split partials use the workspace
+// layout of the 16-head kernel.
+struct TcDecodeParams {
+  const uint16_t* q_nope;
+  const uint16_t* q_rope;
+  int64_t block_stride;
+  int64_t num_blocks;
+  const int32_t* block_table;
+  int max_blocks_per_req;
+  const int32_t* context_lens;
+  const int32_t* topk_idx;
+  int pairs;
+  int q_len;
+  int num_heads;
+  int topk;
+  int splits;
+  float softmax_scale;
+  uint16_t* out;
+  float* lse;
+  void* part_o;
+  float* part_lse;
+  unsigned int* fault_word;
+};
+bool sparse_decode_tc_supported(int fmt, int num_heads);
+int plan_sparse_decode_tc(int pairs, int num_heads, int topk, int max_splits);
+cudaError_t launch_sparse_decode_tc(const TcDecodeParams& p, const CUtensorMap& map, cudaStream_t stream);
+
 // Indexer and top-k.
 size_t topk_workspace_bytes(int batch, int max_context_len, int topk);
 cudaError_t launch_topk(const float* scores, int64_t row_stride, const int32_t* context_lens, int batch, int topk,

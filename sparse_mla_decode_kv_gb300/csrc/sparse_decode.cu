@@ -857,8 +857,37 @@ cudaError_t launch_sparse_decode(int fmt, const uint16_t* q_nope, const uint16_t
     a.part_o = static_cast<__half*>(workspace);
     a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + o_bytes);
   }
-  cudaError_t e = fmt == 0 ? launch_fmt<0>(a, pairs, stream) : launch_fmt<1>(a, pairs, stream);
-  if (e != cudaSuccess || plan.splits == 1 || plan.cluster) return e;
+  int merge_splits = plan.cluster ? 1 : plan.splits;
+  cudaError_t e = cudaSuccess;
+  CUtensorMap tc_map;
+  if (sparse_decode_tc_supported(fmt, num_heads) &&
+      make_row_tensor_map(&tc_map, pool, block_stride, num_blocks, kRowNvfp4)) {
+    TcDecodeParams p;
+    p.q_nope = q_nope;
+    p.q_rope = q_rope;
+    p.block_stride = block_stride;
+    p.num_blocks = num_blocks;
+    p.block_table = block_table;
+    p.max_blocks_per_req = max_blocks_per_req;
+    p.context_lens = context_lens;
+    p.topk_idx = topk_idx;
+    p.pairs = pairs;
+    p.q_len = q_len;
+    p.num_heads = num_heads;
+    p.topk = topk;
+    p.splits = plan_sparse_decode_tc(pairs, num_heads, topk, plan.splits);
+    p.softmax_scale = softmax_scale;
+    p.out = out;
+    p.lse = lse;
+    p.part_o = a.part_o;
+    p.part_lse = a.part_lse;
+    p.fault_word = a.fault_word;
+    merge_splits = p.splits;
+    e = launch_sparse_decode_tc(p, tc_map, stream);
+  } else {
+    e = fmt == 0 ? launch_fmt<0>(a, pairs, stream) : launch_fmt<1>(a, pairs, stream);
+  }
+  if (e != cudaSuccess || merge_splits == 1) return e;
   const int64_t n_bh = static_cast<int64_t>(pairs) * num_heads;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(n_bh));
@@ -871,7 +900,7 @@ cudaError_t launch_sparse_decode(int fmt, const uint16_t* q_nope, const uint16_t
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, splitk_merge_kernel, static_cast<const __half*>(a.part_o),
-                         static_cast<const float*>(a.part_lse), plan.splits, out, lse);
+                         static_cast<const float*>(a.part_lse), merge_splits, out, lse);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
