@@ -12,8 +12,9 @@
 //   * warp 9 allocates 512 tensor-memory columns and one lane issues every
 //     tcgen05.mma;
 //   * warps 0-7 unpack the raw rows into f16 operand chunks in shared
-//     memory (16 KB each, two buffers), run the online softmax and write the
-//     output.
+//     memory (16 KB each, three buffers; a chunk is converted in registers
+//     before its buffer is waited for), run the online softmax and write
+//     the output.
 // Per stage:
 //   S[128 rows x 64 heads] = K[128 x 576] . Q^T   (M = 128, N = 64, 36 MMAs:
 //       nine 64-dim chunks of the rows, K-major; Q K-major, resident)
@@ -47,6 +48,7 @@ constexpr int kTcThreads = kTcUnpackThreads + 64;  // + producer warp + MMA warp
 constexpr int kTcQkChunks = 9;                     // 8 x 64 latent dims + 64 rope dims
 constexpr int kTcPvChunks = 8;                     // 2 row halves x 4 blocks of 128 dims
 constexpr int kTcChunkBytes = 16384;
+constexpr int kTcChunkBufs = 3;
 constexpr int kTcQBytes = kTcHeads * (kLatent + kRope) * 2;  // 73,728
 constexpr int kTcQHeadGroupBytes = (kLatent + kRope) / 8 * 128;  // 9,216: 8 heads x 576 dims
 constexpr int kTcRawBytes = kTcRows * kRowNvfp4;                // 45,056
@@ -81,13 +83,13 @@ struct TcArgs {
 struct alignas(1024) TcSmem {
   uint8_t q_op[kTcQBytes];               // Q, K-major core matrices: (h/8)*9216 + (d/8)*128 + (h%8)*16
   uint8_t raw[2][kTcRawBytes];           // gathered rows, back to back
-  uint8_t chunk[2][kTcChunkBytes];       // unpacked operand chunks
+  uint8_t chunk[kTcChunkBufs][kTcChunkBytes];  // unpacked operand chunks
   uint8_t p_op[kTcPBytes];               // P, MN-major: (h/8)*2048 + (r/8)*128 + (r%8)*16 + (h%8)*2
   int32_t tok[2][kTcRows];               // token of each row of the slot's stage, -1 if masked
   float red[kTcUnpackWarps][32];         // per-warp, per-head reduction scratch
   float m_ref[2][32];                    // running (lazy) maximum per head, base 2, per head half
   float alpha[2][32];                    // rescale factor of the last raise, per head half
-  uint64_t raw_full[2], raw_free[2], chunk_full[2], chunk_free[2], s_full, p_full, done;
+  uint64_t raw_full[2], raw_free[2], chunk_full[kTcChunkBufs], chunk_free[kTcChunkBufs], s_full, p_full, done;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -156,6 +158,17 @@ __device__ __forceinline__ bool bar_red_or(bool pred, int threads) {
   return out != 0;
 }
 
+// The same, polling without the suspend hint: for the chunk hand-offs, where
+// the phase usually completes within a few hundred cycles.
+__device__ __forceinline__ bool tc_wait_spin(TcSmem& sm, uint64_t* bar, uint32_t parity, unsigned int* fault_word) {
+  for (uint32_t i = 0; i < (1u << 26); ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 63 && *reinterpret_cast<volatile int*>(&sm.abort_flag)) return false;
+  }
+  atomicOr(fault_word, kFaultDecodeWait);
+  *reinterpret_cast<volatile int*>(&sm.abort_flag) = 1;
+  return false;
+}
 // Bounded wait that also gives up as soon as another role has aborted.
 __device__ __forceinline__ bool tc_wait(TcSmem& sm, uint64_t* bar, uint32_t parity, unsigned int* fault_word) {
   for (uint32_t i = 0; i < kSpinPolls; ++i) {
@@ -202,6 +215,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.raw_full[i], 1);
       mbar_init(&sm.raw_free[i], kTcUnpackThreads);
+    }
+    for (int i = 0; i < kTcChunkBufs; ++i) {
       mbar_init(&sm.chunk_full[i], kTcUnpackThreads);
       mbar_init(&sm.chunk_free[i], 1);
     }
@@ -292,8 +307,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int s = 0; s < n_stages && ok; ++s) {
         // S = K . Q^T over nine 64-dim chunks (four K = 16 steps each)
         for (int c = 0; c < kTcQkChunks; ++c, ++q) {
-          const int bb = q & 1;
-          ok = tc_wait(sm, &sm.chunk_full[bb], static_cast<uint32_t>(q >> 1) & 1u, fw);
+          const int bb = q % kTcChunkBufs;
+          ok = tc_wait_spin(sm, &sm.chunk_full[bb], static_cast<uint32_t>(q / kTcChunkBufs) & 1u, fw);
           if (!ok) break;
           tc_fence_after();
           const uint32_t a0 = ch_base0 + bb * kTcChunkBytes;
@@ -311,8 +326,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // O^T += V^T . P^T: row half hf, 128-dim block blk (four K = 16 steps)
         for (int c = 0; c < kTcPvChunks; ++c, ++q) {
           const int hf = c >> 2, blk = c & 3;
-          const int bb = q & 1;
-          ok = tc_wait(sm, &sm.chunk_full[bb], static_cast<uint32_t>(q >> 1) & 1u, fw);
+          const int bb = q % kTcChunkBufs;
+          ok = tc_wait_spin(sm, &sm.chunk_full[bb], static_cast<uint32_t>(q / kTcChunkBufs) & 1u, fw);
           if (!ok) break;
           tc_fence_after();
           const uint32_t a0 = ch_base0 + bb * kTcChunkBytes;
@@ -348,16 +363,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // core matrices (r/8)*1024 + (d/8)*128 + (r%8)*16; lane -> row r with
       // r % 8 = lane % 8 (conflict-free 16-byte stores), 8-dim group lane / 8
       for (int c = 0; c < kTcQkChunks; ++c, ++q) {
-        const int bb = q & 1;
-        if (ok && q >= 2) ok = tc_wait(sm, &sm.chunk_free[bb], static_cast<uint32_t>((q >> 1) + 1) & 1u, fw);
-        if (!ok) continue;
-        uint8_t* dst = sm.chunk[bb];
+        const int bb = q % kTcChunkBufs;
+        uint32_t hvs[4][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int r = 8 * (w + 8 * (i & 1)) + t_lo;
           const int dg = dg_lo + 4 * (i >> 1);
           const uint8_t* row = raw + r * kRowNvfp4;
-          uint32_t hv[4];
+          uint32_t (&hv)[4] = hvs[i];
           if (c < 8) {
             const uint32_t codes = *reinterpret_cast<const uint32_t*>(row + 32 * c + 4 * dg);
             const uint32_t s2 = e4m3x2_to_f16x2(static_cast<uint32_t>(row[kScaleOff + 4 * c + (dg >> 1)]) * 0x0101u);
@@ -374,8 +387,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             hv[2] = hi[0];
             hv[3] = hi[1];
           }
+        }
+        if (ok && q >= kTcChunkBufs)
+          ok = tc_wait_spin(sm, &sm.chunk_free[bb], static_cast<uint32_t>(q / kTcChunkBufs + 1) & 1u, fw);
+        if (!ok) continue;
+        uint8_t* dst = sm.chunk[bb];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = 8 * (w + 8 * (i & 1)) + t_lo;
+          const int dg = dg_lo + 4 * (i >> 1);
           *reinterpret_cast<uint4*>(dst + (r >> 3) * 1024 + dg * 128 + (r & 7) * 16) =
-              make_uint4(hv[0], hv[1], hv[2], hv[3]);
+              make_uint4(hvs[i][0], hvs[i][1], hvs[i][2], hvs[i][3]);
         }
         fence_async_smem();
         mbar_arrive(&sm.chunk_full[bb]);
@@ -468,23 +490,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // 128 blk + 127, MN-major core matrices (d/8)*1024 + (r/8)*128 + (r%8)*16
       for (int c = 0; c < kTcPvChunks; ++c, ++q) {
         const int hf = c >> 2, blk = c & 3;
-        const int bb = q & 1;
-        if (ok && q >= 2) ok = tc_wait(sm, &sm.chunk_free[bb], static_cast<uint32_t>((q >> 1) + 1) & 1u, fw);
-        if (!ok) continue;
-        uint8_t* dst = sm.chunk[bb];
+        const int bb = q % kTcChunkBufs;
         const int rr = 8 * w + t_lo;
         const uint8_t* row = raw + (64 * hf + rr) * kRowNvfp4;
+        uint32_t hvs[4][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int dg = dg_lo + 4 * i;
           const uint32_t codes = *reinterpret_cast<const uint32_t*>(row + 64 * blk + 4 * dg);
           const uint32_t s2 = e4m3x2_to_f16x2(static_cast<uint32_t>(row[kScaleOff + 8 * blk + (dg >> 1)]) * 0x0101u);
-          uint32_t hv[4];
-          e2m1x8_to_f16x2x4(codes, hv);
+          e2m1x8_to_f16x2x4(codes, hvs[i]);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) hv[k] = hmul2(hv[k], s2);
-          *reinterpret_cast<uint4*>(dst + dg * 1024 + rr * 16) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+          for (int k = 0; k < 4; ++k) hvs[i][k] = hmul2(hvs[i][k], s2);
         }
+        if (ok && q >= kTcChunkBufs)
+          ok = tc_wait_spin(sm, &sm.chunk_free[bb], static_cast<uint32_t>(q / kTcChunkBufs + 1) & 1u, fw);
+        if (!ok) continue;
+        uint8_t* dst = sm.chunk[bb];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<uint4*>(dst + (dg_lo + 4 * i) * 1024 + rr * 16) =
+              make_uint4(hvs[i][0], hvs[i][1], hvs[i][2], hvs[i][3]);
         fence_async_smem();
         mbar_arrive(&sm.chunk_full[bb]);
       }
