@@ -5,25 +5,25 @@
  *
  * What the operations are, and where they are defined:
  *
- *  - The cached row.  Each token caches one 512-value latent plus one
- *    64-value rotary key, with no head axis; every attention head reads the
+ *  - The cached row.  A token's cache entry is a 512-value latent and a
+ *    64-value rotary key shared by all heads (no head axis); every attention head reads the
  *    same row ("Prime Inference: serving GLM-5.3 to agents is a KV-cache
  *    problem", section "Prefill topology").  Stored as NVFP4 it is 256 bytes
  *    of 4-bit e2m1 codes, 32 one-byte e4m3 scales (one per 16 latent values)
  *    and 64 one-byte e4m3 rope values = 352 bytes; stored as FP8 it is 512 +
  *    64 e4m3 bytes = 576 bytes (same page, section "Four bits per latent
  *    value: where 352 comes from", row table).
- *  - Sparse selection.  An indexer scores every earlier token and attention
+ *  - Sparse selection.  The indexer rates all preceding tokens and attention
  *    reads at most top-k = 2,048 of them ("GLM-5.3 PCP/DCP long-context on
  *    H200", section 1; "Prime Inference", section "Decode: TP4, and the
- *    copies it keeps", index_topk 2048).  Indexer keys are 128 FP8 values
- *    plus a 4-byte scale per token (PCP/DCP page, section 3).
+ *    copies it keeps", index_topk 2048).  An indexer key is 128 e4m3 bytes
+ *    and a float scale (PCP/DCP page, section 3).
  *  - Decode.  The selected rows are gathered through the block table,
  *    unpacked on chip, scored against every head's absorbed query, soft-maxed
  *    and blended, with no FP8 or BF16 copy written to memory ("Prime
  *    Inference", section "A kernel that reads four bits directly", figure
- *    "staged vs native decode"); short contexts leave -1 entries in the
- *    top-k list, which are skipped (same section).
+ *    "staged vs native decode"); when a context is shorter than top-k the
+ *    list carries -1 entries, which are skipped (same section).
  *
  * Row layout inside the 352 bytes (the pages give only the totals):
  *   [0,256)   latent codes, element 2i in the low nibble of byte i
@@ -114,7 +114,7 @@ mla_status_t mla_kv_quantize_append(const uint16_t* latent, const uint16_t* rope
 
 /*
  * Quantize-on-write of the indexer's keys ("GLM-5.3 PCP/DCP long-context on
- * H200", section 3: 128 FP8 values plus a 4-byte scale per token).  Per
+ * H200", section 3: a key is 128 e4m3 bytes and a float scale).  Per
  * token: s = max_d |k_d| / 448 and code_d = e4m3_rn_satfinite(k_d / s), both
  * divisions IEEE float32; a key whose values are all zero stores s = 0 and
  * 128 zero codes.  Block layout (the layout mla_indexer_topk reads): block b
@@ -242,7 +242,7 @@ mla_status_t mla_sparse_decode_fp8(const uint16_t* q_nope, const uint16_t* q_rop
 /*
  * Several query tokens per request, decoded in one launch (speculative draft
  * tokens: "Prime Inference", section "A kernel that reads four bits
- * directly" -- the native kernel runs 15 query tokens per launch).  Each
+ * directly" -- the native kernel handles 15 query tokens in one launch).  Each
  * query token has its own top-k list; the q_len tokens of request b are the
  * last q_len positions of its context_lens[b] tokens, so token i sees only
  * t < context_lens[b] - (q_len - 1 - i) (entries at or past that bound are
@@ -309,7 +309,7 @@ mla_status_t mla_sparse_decode_staged(const uint16_t* q_nope, const uint16_t* q_
 
 /*
  * Exact top-k over float scores ("GLM-5.3 PCP/DCP long-context on H200",
- * section 1: sparse MLA attends to the 2,048 tokens the indexer picks).
+ * section 1: attention reads only the 2,048 tokens the indexer rates best).
  * For request b the candidates are t in [0, min(context_lens[b],
  * max_context_len)), ordered by (score descending, t ascending), with -0.0
  * equal to +0.0; the first min(k, n) are written to topk_out[b, :] in
@@ -334,8 +334,8 @@ mla_status_t mla_topk(const float* scores, int64_t score_row_stride, const int32
  *   score[b,t] = sum_h head_w[b,h] * max(0, s_t * (q_idx[b,h] . k_t))
  *
  * where k_t is the token's 128 e4m3 key values and s_t its float scale
- * ("GLM-5.3 PCP/DCP long-context on H200", section 3: 128 FP8 values plus a
- * 4-byte scale per token); then topk_out = mla_topk(score).  Tensor-core
+ * ("GLM-5.3 PCP/DCP long-context on H200", section 3: a key is 128 e4m3
+ * bytes and a float scale); then topk_out = mla_topk(score).  Tensor-core
  * products use FP16 operands (keys exact; q converted from bf16 with
  * saturation) with FP32 accumulation.
  *

@@ -18,11 +18,11 @@
  *       section "Prefill topology" (512-value latent + 64-value rotary key,
  *       all heads up-project from the same latent).
  *  [P3] Prime Intellect's own post (aioga.com copy), paragraphs on NVFP4:
- *       "four bits per value, with an FP8 scale for each group of 16 values",
- *       "the 64-value positional component remained FP8".
- *  [P5] "GLM-5.3 PCP/DCP long-context on H200", section 1 (indexer scores
- *       every earlier token; sparse MLA attends to the 2,048 it picks) and
- *       section 3 (indexer keys: 128 FP8 values + a 4-byte scale per token).
+ *       the latent is stored as 4-bit values with one FP8 scale per 16 of
+ *       them, and the 64 positional values are kept in FP8.
+ *  [P5] "GLM-5.3 PCP/DCP long-context on H200", section 1 (the indexer
+ *       rates all preceding tokens and attention reads only the 2,048 best)
+ *       and section 3 (an indexer key is 128 e4m3 bytes and a float scale).
  *  Number formats the pages name but do not print: OCP 8-bit floating point
  *  specification (E4M3, "fn" variant: no infinities, S.1111.111 = NaN, max
  *  448) and OCP Microscaling Formats (MX) v1.0 (FP4 E2M1: values 0, 0.5, 1,
@@ -402,8 +402,8 @@ void oracle_sparse_decode_mtp(const uint16_t* q_nope, const uint16_t* q_rope, co
 
 /* score[t] = sum_h w[h] * max(0, s_t * (q[h] . k_t)) for t in [0, ctx), where
  * k_t are 128 e4m3 values and s_t a float scale, found through the block
- * table (R-keys).  [P5 section 1: "an indexer scores every earlier token";
- * section 3: 128 FP8 values plus a 4-byte scale per token]. */
+ * table (R-keys).  [P5 section 1: the indexer rates every preceding token;
+ * section 3: a key is 128 e4m3 bytes and a float scale]. */
 void oracle_indexer_scores_request(const uint16_t* q_idx, const float* head_w, int n_idx_heads,
                                    const uint8_t* idx_key_pool, int64_t idx_block_stride,
                                    const int32_t* block_table_row, int context_len, int block_size,
@@ -427,7 +427,7 @@ void oracle_indexer_scores_request(const uint16_t* q_idx, const float* head_w, i
 }
 
 /* One token's 128 bf16 indexer-key values -> 128 e4m3 codes and a float
- * scale [P5 section 3: 128 FP8 values plus a 4-byte scale per token].
+ * scale [P5 section 3: a key is 128 e4m3 bytes and a float scale].
  * R-keyscale: s = amax / 448 and code_d = e4m3_rn_satfinite(k_d / s), both
  * divisions in IEEE single precision (the precision of the stored scale, so
  * every rounding decision is taken on a float).  amax = 0 stores s = 0 and

@@ -1,8 +1,8 @@
 // Indexer score and exact top-k selection.
 //
-// "GLM-5.3 PCP/DCP long-context on H200", section 1: an indexer scores every
-// earlier token and sparse MLA attends to the 2,048 it picks; section 3:
-// indexer keys are 128 FP8 values plus a 4-byte scale per token.  The score
+// "GLM-5.3 PCP/DCP long-context on H200", section 1: the indexer rates all
+// preceding tokens and attention reads only the 2,048 best; section 3: an
+// indexer key is 128 e4m3 bytes and a float scale.  The score
 // is sum_h w_h * relu(s_t * (q_h . k_t)).
 //
 // indexer_scores_kernel: one CTA = 4 warps over 512 tokens of one request.

@@ -108,8 +108,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   }
 }
 
-// Indexer keys ("GLM-5.3 PCP/DCP long-context on H200", section 3: 128 FP8
-// values plus a 4-byte scale per token): s = amax / 448 and codes
+// Indexer keys ("GLM-5.3 PCP/DCP long-context on H200", section 3: a key is
+// 128 e4m3 bytes and a float scale): s = amax / 448 and codes
 // e4m3(k / s), both divisions IEEE single precision; a zero key stores s = 0
 // and zero codes.  Four lanes per token: lane l of the four owns values
 // [32l, 32l+32) (four 16-byte loads, two 16-byte stores), so the per-token

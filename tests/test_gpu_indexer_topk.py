@@ -1,8 +1,8 @@
 """Indexer score and exact top-k on the GPU against the oracle.
 
-Sources: "GLM-5.3 PCP/DCP long-context on H200", section 1 (an indexer
-scores every earlier token; sparse MLA attends to the top 2,048) and section
-3 (keys: 128 FP8 values plus a 4-byte scale per token); "Prime Inference:
+Sources: "GLM-5.3 PCP/DCP long-context on H200", section 1 (the indexer
+rates all preceding tokens; attention reads the best 2,048) and section 3 (a
+key is 128 e4m3 bytes and a float scale); "Prime Inference:
 serving GLM-5.3 to agents is a KV-cache problem", section "Decode: TP4"
 (index_topk 2048).
 

@@ -1,8 +1,8 @@
 """Indexer-key quantize-on-write and the staged NVFP4 -> FP8 path on the GPU
 against the oracle.
 
-Keys: "GLM-5.3 PCP/DCP long-context on H200", section 3 (128 FP8 values plus
-a 4-byte scale per token) -- byte-exact.  Staged path: "Prime Inference:
+Keys: "GLM-5.3 PCP/DCP long-context on H200", section 3 (a key is 128 e4m3
+bytes and a float scale) -- byte-exact.  Staged path: "Prime Inference:
 serving GLM-5.3 to agents is a KV-cache problem", section "A kernel that
 reads four bits directly", figure "staged vs native decode" -- the staged
 rows and list are byte-exact; the staged decode is held to the decode

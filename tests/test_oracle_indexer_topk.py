@@ -1,8 +1,8 @@
 """Pins for the oracle's indexer score and exact top-k (CPU only).
 
-Source: "GLM-5.3 PCP/DCP long-context on H200", section 1 (an indexer scores
-every earlier token and sparse MLA attends to the 2,048 it picks) and section
-3 (indexer keys: 128 FP8 values plus a 4-byte scale per token); "Prime
+Source: "GLM-5.3 PCP/DCP long-context on H200", section 1 (the indexer rates
+all preceding tokens and attention reads only the 2,048 best) and section 3
+(an indexer key is 128 e4m3 bytes and a float scale); "Prime
 Inference: serving GLM-5.3 to agents is a KV-cache problem", section "Decode:
 TP4, and the copies it keeps" (index_topk 2048).  The score formula
 sum_h w_h * relu(s_t * (q_h . k_t)) is the workload definition this library

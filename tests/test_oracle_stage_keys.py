@@ -4,8 +4,8 @@ Staged path: "Prime Inference: serving GLM-5.3 to agents is a KV-cache
 problem", section "A kernel that reads four bits directly", figure "staged vs
 native decode" (a gather kernel reads the 352-byte NVFP4 rows and writes a
 576-byte FP8 copy that an FP8 attention kernel then reads).  Indexer keys:
-"GLM-5.3 PCP/DCP long-context on H200", section 3 (128 FP8 values plus a
-4-byte scale per token).
+"GLM-5.3 PCP/DCP long-context on H200", section 3 (a key is 128 e4m3 bytes
+and a float scale).
 
 Every check compares the oracle with something other than its own
 arithmetic: the OCP tables through torch's float8_e4m3fn decoder, a

@@ -3,8 +3,8 @@
 Sources: "Prime Inference: serving GLM-5.3 to agents is a KV-cache problem",
 sections "Four bits per latent value: where 352 comes from" (1.64x per row,
 (576 + x) / (352 + x) = 1.495 gives x ~ 100, 1.09M -> 1.63M tokens, 6.6 / 4.0
-GB sessions), "A kernel that reads four bits directly" (figure: staged path
-touches 352 + 576 + 576 = 1,504 B per selected row, 4.3x) and "Moving the
+GB sessions), "A kernel that reads four bits directly" (figure: 1,504 B =
+352 + 576 + 576 per selected row on the staged path, 4.3x the native 352) and "Moving the
 cache" (5.5 GB for a 200K-token request); "GLM-5.3 PCP/DCP long-context on
 H200", section 1 footnote (26 vs 191 FLOP/B, ridge ~206) and section 3
 (54,728 B per token, 53.4 GiB at 1M tokens, 6.7 GiB with DCP8).

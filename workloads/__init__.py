@@ -6,10 +6,10 @@ quantization, no scoring, no attention.  Both the CUDA path's tests/bench and
 the oracle consume what it returns.
 
 Shapes follow "Prime Inference: serving GLM-5.3 to agents is a KV-cache
-problem" (section "The workload": a turn adds about 6K tokens to a 140K-token
-prompt; section "Decode: TP4": 64 heads split four ways -> 16 per rank,
+problem" (section "The workload": each agent turn appends roughly 6,000 new tokens
+after a roughly 140,000-token prefix; section "Decode: TP4": 64 heads split four ways -> 16 per rank,
 top-k 2,048) and "GLM-5.3 PCP/DCP long-context on H200" (1M-token contexts,
-all 64 heads per DP rank, indexer keys of 128 FP8 values plus a scale).  The
+all 64 heads per DP rank, indexer keys of 128 e4m3 bytes and a float scale).  The
 AgentX traces the pages benchmark on are not available; these seeded draws
 stand in for them.
 
