@@ -61,6 +61,7 @@ def small_draft_workload(batch, heads, topk, ctx_lens, q_len, seed):
     (2, 32, 2048, [9000, 2050], 3),
     (2, 16, 64, [3, 1], 4),          # context shorter than q_len: early tokens see nothing
     (1, 64, 97, [4096], 15),
+    (2, 64, 2048, [9000, 2050], 3),  # 64-head blocks on NVFP4: tensor-memory kernel, split lists
 ])
 def test_drafts_against_oracle(fmt, batch, heads, topk, ctx_lens, q_len):
     m = lib()

@@ -51,11 +51,13 @@ def test_no_alloc_decode_matches_workspace_decode_twice():
     m = lib()
     assert m.mla_sparse_decode_workspace_size(32, 16, 2048) <= 16 << 20
     # 8 splits (merged inside a thread-block cluster), 32 and 64 splits
-    # (merged by a second kernel)
+    # (merged by a second kernel), and 64 heads (the tensor-memory kernel,
+    # its split lists merged by the second kernel)
     cases = [
         build_case(m, lambda: W.tiny_decode(DEV, seed=3)),
         build_case(m, lambda: W.tp4_rank_decode(DEV, seed=5, batch=8, ctx=20_000)),
         build_case(m, lambda: W.tp4_rank_decode(DEV, seed=6, batch=2, ctx=9_000)),
+        build_case(m, lambda: W.tp4_rank_decode(DEV, seed=7, batch=2, ctx=9_000, heads=64)),
     ]
     for wl in cases:  # calls in a row, different shapes sharing the scratch
         assert m.mla_sparse_decode_workspace_size(wl.batch, wl.heads, wl.topk) > 0  # the scratch is used
