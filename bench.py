@@ -100,6 +100,25 @@ def decode_traffic():
     return t["bytes"] if kernel_source_digest() == t["source_digest"] else None
 
 
+GB300_L2_BYTES = 132 * 2 ** 20  # used only when no GPU is visible (reference arm on a host without one)
+
+
+def step_config(ctx, layers, l2_bytes, world):
+    """The `config` of the JSON line, shared by both arms so that the driver
+    compares like with like."""
+    layer_bytes = decode_bytes(32, 16, 2048, ROW_NVFP4)
+    return {"workload": f"TP4 rank decode: 32 requests x 16 heads, {ctx:,}-token contexts, top-2048 "
+                        "(70% prefix + 30% last 6,000), NVFP4 352-byte rows, block 64",
+            "layers_per_step": layers, "block_table": "one per request, shared by the layers",
+            "l2": f"inputs larger than L2: {layers} distinct layer caches, "
+                  f"{layers * layer_bytes / 1e6:.0f} MB read per step vs {l2_bytes / 1e6:.0f} MB L2",
+            "global_batch": 32 * world, "seq_len": ctx, "parallelism": f"replicas x{world}"}
+
+
+def layers_per_step(requested, l2_bytes):
+    return requested or max(8, math.ceil(4 * l2_bytes / decode_bytes(32, 16, 2048, ROW_NVFP4)))
+
+
 def decode_bytes(batch, heads, topk, row_bytes):
     """Algorithmic bytes of one decode layer: every selected row plus its int32
     index, and per (request, head) the bf16 query (576 values), bf16 output
@@ -228,7 +247,14 @@ def run_reference(args, rank, world):
     import oracle as O
     if rank != 0:
         return
-    batch, heads, topk, ctx = 32, 16, 2048, 140_000
+    batch, heads, topk, ctx = 32, 16, 2048, args.ctx
+    l2 = GB300_L2_BYTES
+    try:
+        import torch
+        if torch.cuda.is_available():
+            l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    except Exception:
+        pass
     rng = np.random.default_rng(0)
     threads = O.host_threads()
     # Bounded sample per step: 8 requests' decodes of one layer (float64), rows
@@ -260,10 +286,10 @@ def run_reference(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "TP4 rank decode, 16 heads, top-2048 rows of 352 B (float64 CPU oracle)",
-                       "sample": f"{n_req} requests x {topk} rows per step"},
+            "config": step_config(args.ctx, layers_per_step(args.layers, l2), l2, world),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                             "sample": f"{n_req} of 32 requests of one layer per step, {threads} host threads"},
+                             "sample": f"{n_req} of 32 requests of one layer per step ({n_req} x {topk} rows), "
+                                       f"float64, {threads} host threads"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -305,7 +331,7 @@ def main():
     B, H, K = 32, 16, 2048
     layer_bytes4 = decode_bytes(B, H, K, ROW_NVFP4)
     layer_bytes8 = decode_bytes(B, H, K, ROW_FP8)
-    L = args.layers or max(8, math.ceil(4 * l2 / layer_bytes4))
+    L = layers_per_step(args.layers, l2)
 
     def qa(lat, rope, slots, pool, nb, stride, fmt):
         m.mla_kv_quantize_append(lat, rope, slots, pool, nb, 64, stride, fmt)
@@ -515,13 +541,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms4, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": {"workload": f"TP4 rank decode: 32 requests x 16 heads, {args.ctx:,}-token contexts, top-2048 "
-                               "(70% prefix + 30% last 6,000), NVFP4 352-byte rows, block 64",
-                   "layers_per_step": L, "block_table": "one per request, shared by the layers",
-                   "l2": f"inputs larger than L2: {L} distinct layer caches, "
-                                              f"{L * layer_bytes4 / 1e6:.0f} MB read per step vs "
-                                              f"{l2 / 1e6:.0f} MB L2",
-                   "global_batch": B * world, "seq_len": args.ctx, "parallelism": f"replicas x{world}"},
+        "config": step_config(args.ctx, L, l2, world),
         "per_layer_us": per_layer4 * 1e6,
         "hbm_gbs": ach4,
         "roofline": {"bound": "hbm" if layer_bytes4 / hbm / 1e9 >= fl / tf_burst / 1e12 else "tensor",
