@@ -233,23 +233,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  if (warp < kTcUnpackWarps) {
-    // The absorbed query of the 64 heads, bf16 -> f16, as K-major core
-    // matrices: 8 heads x 8 dims per 128 bytes.
-    const int64_t qrow = static_cast<int64_t>(v) * args.num_heads + h0;
-    constexpr int kDimGroups = (kLatent + kRope) / 8;
-    for (int u = threadIdx.x; u < kTcHeads * kDimGroups; u += kTcUnpackThreads) {
-      const int h = u / kDimGroups;
-      const int dg = u - h * kDimGroups;
-      const uint4 x = dg < kLatent / 8
-                          ? __ldg(reinterpret_cast<const uint4*>(args.q_nope + (qrow + h) * kLatent) + dg)
-                          : __ldg(reinterpret_cast<const uint4*>(args.q_rope + (qrow + h) * kRope) + (dg - kLatent / 8));
-      *reinterpret_cast<uint4*>(sm.q_op + (h >> 3) * kTcQHeadGroupBytes + dg * 128 + (h & 7) * 16) =
-          make_uint4(tc_bf16pair_to_f16x2(x.x), tc_bf16pair_to_f16x2(x.y), tc_bf16pair_to_f16x2(x.z),
-                     tc_bf16pair_to_f16x2(x.w));
-    }
-    fence_async_smem();
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -353,6 +336,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
     for (int j = 0; j < 32; ++j) l_part[j] = 0.f;
     const float* m_ref = sm.m_ref[half];
+    {
+      // The absorbed query of the 64 heads, bf16 -> f16, as K-major core
+      // matrices (8 heads x 8 dims per 128 bytes); all loads issued before
+      // any is used, while the producer gathers the first stage.  The proxy
+      // fence before the first chunk's arrival publishes it to the MMAs.
+      const int64_t qrow = static_cast<int64_t>(v) * args.num_heads + h0;
+      constexpr int kDimGroups = (kLatent + kRope) / 8;
+      constexpr int kQPer = kTcHeads * kDimGroups / kTcUnpackThreads;  // 18
+      uint4 xs[kQPer];
+#pragma unroll
+      for (int i = 0; i < kQPer; ++i) {
+        const int u = threadIdx.x + i * kTcUnpackThreads;
+        const int h = u / kDimGroups;
+        const int dg = u - h * kDimGroups;
+        xs[i] = dg < kLatent / 8
+                    ? __ldg(reinterpret_cast<const uint4*>(args.q_nope + (qrow + h) * kLatent) + dg)
+                    : __ldg(reinterpret_cast<const uint4*>(args.q_rope + (qrow + h) * kRope) + (dg - kLatent / 8));
+      }
+#pragma unroll
+      for (int i = 0; i < kQPer; ++i) {
+        const int u = threadIdx.x + i * kTcUnpackThreads;
+        const int h = u / kDimGroups;
+        const int dg = u - h * kDimGroups;
+        *reinterpret_cast<uint4*>(sm.q_op + (h >> 3) * kTcQHeadGroupBytes + dg * 128 + (h & 7) * 16) =
+            make_uint4(tc_bf16pair_to_f16x2(xs[i].x), tc_bf16pair_to_f16x2(xs[i].y),
+                       tc_bf16pair_to_f16x2(xs[i].z), tc_bf16pair_to_f16x2(xs[i].w));
+      }
+      fence_async_smem();
+    }
     int q = 0;
     bool aborted = false;
     for (int s = 0; s < n_stages; ++s) {
