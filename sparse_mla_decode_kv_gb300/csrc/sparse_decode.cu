@@ -857,6 +857,10 @@ cudaError_t launch_sparse_decode(int fmt, const uint16_t* q_nope, const uint16_t
     a.part_o = static_cast<__half*>(workspace);
     a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + o_bytes);
   }
+  // 64-head blocks of NVFP4 rows in a pool TMA can describe go to the
+  // tensor-memory kernel; it splits a list at most plan.splits ways, so the
+  // workspace sized for this plan holds its partials (same layout), which
+  // the merge kernel below combines.
   int merge_splits = plan.cluster ? 1 : plan.splits;
   cudaError_t e = cudaSuccess;
   CUtensorMap tc_map;
