@@ -249,13 +249,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int row_end = min(args.topk, row_begin + args.rows_per_split);
   const int n_rows = max(0, row_end - row_begin);
   const int n_stages = (n_rows + kStageRows - 1) / kStageRows;
-  // query token i of the request's q_len sees t < ctx_b - (q_len - 1 - i)
-  const int ctx = __ldg(args.ctx_lens + b) - (args.q_len - 1 - (v - b * args.q_len));
 
   // This grid is launched as a programmatic dependent of whatever precedes it
   // on the stream: its CTAs may be resident early, but nothing is read before
   // the preceding grid has completed and its writes are visible.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // query token i of the request's q_len sees t < ctx_b - (q_len - 1 - i)
+  const int ctx = __ldg(args.ctx_lens + b) - (args.q_len - 1 - (v - b * args.q_len));
   // The split merge (launched as a programmatic dependent) may start its
   // launch now; it waits for this whole grid before reading any partial.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
