@@ -702,7 +702,11 @@ def dep_measurement(m, W, dev, stream, args, hbm):
     bytes_ = rows * (ROW_NVFP4 + 4) + B * H * (576 * 2 + 512 * 2 + 4)
     flops = decode_flops(B, H, K)
     roof = max(bytes_ / (hbm * 1e9), flops / (tf_burst * 1e12))
-    res = {"workload": wl.name, "us": t * 1e6, "rows_per_s": rows / t, "hbm_gbs": bytes_ / t / 1e9,
+    plan = m.mla_sparse_decode_plan_fmt(0, B, H, K, wl.strides[0], wl.num_blocks)
+    kernel = ("sparse_decode_tc_kernel (tcgen05.mma, accumulators in tensor memory)" if plan["tensor_memory"]
+              else "sparse_decode_kernel<NVFP4> (mma.sync)")
+    res = {"workload": wl.name, "kernel": kernel, "plan": plan, "us": t * 1e6, "rows_per_s": rows / t,
+           "hbm_gbs": bytes_ / t / 1e9,
            "tflops": flops / t / 1e12, "tensor_frac_of_bf16_peak": flops / t / 1e12 / tf_burst,
            "roofline_us": roof * 1e6, "frac_of_roofline_time": roof / t}
     del wl, flush, ws

@@ -190,6 +190,21 @@ size_t mla_sparse_decode_workspace_size(int batch, int num_heads, int topk);
  */
 mla_status_t mla_sparse_decode_plan(int batch, int num_heads, int topk, int* splits, int* rows_per_split,
                                     int* kernels);
+
+/*
+ * The division a call with this cache format and pool geometry actually
+ * uses: as mla_sparse_decode_plan, and *tensor_memory = 1 when the call runs
+ * the tensor-memory kernel (fmt MLA_KV_NVFP4, num_heads a multiple of 64,
+ * kv_block_stride a whole number of 352-byte rows, num_blocks > 0 and fewer
+ * than 2^31 pool rows; the pool base 16-byte aligned, as every call
+ * requires).  Its splits are then per (request, 64-head block) with
+ * ceil(topk / splits) rows each, and *kernels is 2 when a merge follows.
+ * Output pointers may be NULL.  MLA_ERR_INVALID_ARG for an unknown fmt or
+ * the arguments mla_sparse_decode_plan rejects.
+ */
+mla_status_t mla_sparse_decode_plan_fmt(int fmt, int batch, int num_heads, int topk, int64_t kv_block_stride,
+                                        int64_t num_blocks, int* splits, int* rows_per_split, int* kernels,
+                                        int* tensor_memory);
 mla_status_t mla_sparse_decode(const uint16_t* q_nope, const uint16_t* q_rope, const void* kv_pool,
                                int64_t kv_block_stride, int64_t num_blocks, const int32_t* block_table,
                                int max_blocks_per_req, const int32_t* context_lens, const int32_t* topk_idx,

@@ -17,7 +17,8 @@ import torch
 __all__ = [
     "MlaError", "MLA_KV_NVFP4", "MLA_KV_FP8", "library_path", "load",
     "mla_kv_row_bytes", "mla_status_string", "mla_last_cuda_error", "mla_device_fault",
-    "mla_kv_quantize_append", "mla_sparse_decode_workspace_size", "mla_sparse_decode_plan", "mla_sparse_decode",
+    "mla_kv_quantize_append", "mla_sparse_decode_workspace_size", "mla_sparse_decode_plan",
+    "mla_sparse_decode_plan_fmt", "mla_sparse_decode",
     "mla_sparse_decode_fp8", "mla_sparse_decode_noalloc", "mla_topk_workspace_size", "mla_topk",
     "mla_indexer_topk_workspace_size", "mla_indexer_topk", "mla_index_key_quantize_append",
     "mla_staged_pool_bytes", "mla_stage_rows_fp8", "mla_sparse_decode_staged_workspace_size",
@@ -43,6 +44,7 @@ SIGNATURES = {
     "mla_kv_quantize_append": (_I32, [_P, _P, _P, _I64, _P, _I64, _I32, _I64, _I32, _P]),
     "mla_sparse_decode_workspace_size": (_SZ, [_I32, _I32, _I32]),
     "mla_sparse_decode_plan": (_I32, [_I32, _I32, _I32, _P, _P, _P]),
+    "mla_sparse_decode_plan_fmt": (_I32, [_I32, _I32, _I32, _I32, _I64, _I64, _P, _P, _P, _P]),
     "mla_sparse_decode": (_I32, [_P, _P, _P, _I64, _I64, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _F32, _P, _P,
                                  _P, _SZ, _P]),
     "mla_sparse_decode_fp8": (_I32, [_P, _P, _P, _I64, _I64, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _F32, _P,
@@ -199,6 +201,17 @@ def mla_sparse_decode_plan(batch: int, num_heads: int, topk: int) -> dict:
            load().mla_sparse_decode_plan(batch, num_heads, topk, C.byref(sp), C.byref(rows), C.byref(kern)))
     return {"splits": sp.value, "rows_per_split": rows.value, "kernels": kern.value}
 
+
+def mla_sparse_decode_plan_fmt(fmt: int, batch: int, num_heads: int, topk: int, kv_block_stride: int,
+                               num_blocks: int) -> dict:
+    """The division a decode with this cache format and pool geometry uses,
+    including whether it runs the tensor-memory kernel."""
+    sp, rows, kern, tm = C.c_int(), C.c_int(), C.c_int(), C.c_int()
+    _check("mla_sparse_decode_plan_fmt",
+           load().mla_sparse_decode_plan_fmt(fmt, batch, num_heads, topk, kv_block_stride, num_blocks, C.byref(sp),
+                                             C.byref(rows), C.byref(kern), C.byref(tm)))
+    return {"splits": sp.value, "rows_per_split": rows.value, "kernels": kern.value,
+            "tensor_memory": bool(tm.value)}
 
 def _decode(cname: str, q_nope, q_rope, kv_pool, kv_block_stride, num_blocks, block_table, context_lens, topk_idx,
             softmax_scale, block_size=64, out=None, lse=None, workspace=None, stream=None,

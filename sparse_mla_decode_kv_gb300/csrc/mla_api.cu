@@ -219,6 +219,26 @@ mla_status_t mla_sparse_decode_plan(int batch, int num_heads, int topk, int* spl
   return MLA_OK;
 }
 
+mla_status_t mla_sparse_decode_plan_fmt(int fmt, int batch, int num_heads, int topk, int64_t kv_block_stride,
+                                        int64_t num_blocks, int* splits, int* rows_per_split, int* kernels,
+                                        int* tensor_memory) {
+  if (fmt != MLA_KV_NVFP4 && fmt != MLA_KV_FP8) return MLA_ERR_INVALID_ARG;
+  if (batch <= 0 || num_heads < 16 || num_heads % 16 != 0 || topk < 1) return MLA_ERR_INVALID_ARG;
+  const DecodePlan plan = plan_sparse_decode(batch, num_heads, topk);
+  const bool tc = sparse_decode_uses_tc(fmt, num_heads, kv_block_stride, num_blocks);
+  int s = plan.splits, rows = plan.rows_per_split, k = (plan.splits > 1 && !plan.cluster) ? 2 : 1;
+  if (tc) {
+    s = plan_sparse_decode_tc(batch, num_heads, topk, plan.splits);
+    rows = (topk + s - 1) / s;
+    k = s > 1 ? 2 : 1;
+  }
+  if (splits) *splits = s;
+  if (rows_per_split) *rows_per_split = rows;
+  if (kernels) *kernels = k;
+  if (tensor_memory) *tensor_memory = tc ? 1 : 0;
+  return MLA_OK;
+}
+
 mla_status_t mla_sparse_decode(const uint16_t* q_nope, const uint16_t* q_rope, const void* kv_pool,
                                int64_t kv_block_stride, int64_t num_blocks, const int32_t* block_table,
                                int max_blocks_per_req, const int32_t* context_lens, const int32_t* topk_idx,

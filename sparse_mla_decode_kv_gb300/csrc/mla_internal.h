@@ -76,6 +76,10 @@ struct TcDecodeParams {
   unsigned int* fault_word;
 };
 bool sparse_decode_tc_supported(int fmt, int num_heads);
+// The call runs the tensor-memory kernel (format, head count and a pool TMA
+// can describe as a tensor of 352-byte rows; the pool base must also be
+// 16-byte aligned, which every entry point already requires).
+bool sparse_decode_uses_tc(int fmt, int num_heads, int64_t block_stride, int64_t num_blocks);
 int plan_sparse_decode_tc(int pairs, int num_heads, int topk, int max_splits);
 cudaError_t launch_sparse_decode_tc(const TcDecodeParams& p, const CUtensorMap& map, cudaStream_t stream);
 

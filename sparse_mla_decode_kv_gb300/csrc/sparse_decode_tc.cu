@@ -598,6 +598,14 @@ bool sparse_decode_tc_supported(int fmt, int num_heads) {
   return fmt == 0 && num_heads >= kTcHeads && num_heads % kTcHeads == 0;
 }
 
+// The same conditions as the dispatch in launch_sparse_decode: the format
+// and head count, and a pool the row tensor map can describe (a stride of
+// whole rows, at least one block, row coordinates within 32 bits).
+bool sparse_decode_uses_tc(int fmt, int num_heads, int64_t block_stride, int64_t num_blocks) {
+  if (!sparse_decode_tc_supported(fmt, num_heads) || num_blocks <= 0 || block_stride % kRowNvfp4 != 0) return false;
+  return num_blocks * (block_stride / kRowNvfp4) <= 0x7FFFFFFF;
+}
+
 int plan_sparse_decode_tc(int pairs, int num_heads, int topk, int max_splits) {
   const int groups = pairs * (num_heads / kTcHeads);
   const int stages = (topk + kTcRows - 1) / kTcRows;

@@ -138,6 +138,32 @@ def test_decode_plan(lib):
     assert lib.mla_sparse_decode_plan(4, 16, 2048, None, None, None) == 0
 
 
+def test_decode_plan_for_format_and_pool(lib):
+    """The format-aware plan says when the tensor-memory kernel runs (NVFP4,
+    64-head blocks, a pool stride of whole 352-byte rows) and then splits a
+    list at most as many ways as the 16-head plan, so its partials fit the
+    same workspace."""
+    import sparse_mla_decode_kv_gb300 as m
+    nvfp4, fp8 = 0, 1
+    packed = 64 * 352
+    for batch, heads, topk in [(128, 64, 2048), (1, 64, 2048), (2, 128, 700), (6, 64, 2048), (3, 64, 1)]:
+        p = m.mla_sparse_decode_plan_fmt(nvfp4, batch, heads, topk, packed, 1000)
+        base = m.mla_sparse_decode_plan(batch, heads, topk)
+        assert p["tensor_memory"]
+        assert 1 <= p["splits"] <= base["splits"]
+        assert p["splits"] * p["rows_per_split"] >= topk and (p["splits"] - 1) * p["rows_per_split"] < topk
+        assert p["kernels"] == (2 if p["splits"] > 1 else 1)
+    # everything else is the 16-head plan
+    for fmt, heads, stride, nb in [(nvfp4, 16, packed, 1000), (nvfp4, 48, packed, 1000), (fp8, 64, 64 * 576, 1000),
+                                   (nvfp4, 64, packed + 16, 1000), (nvfp4, 64, packed, 0)]:
+        p = m.mla_sparse_decode_plan_fmt(fmt, 4, heads, 2048, stride, nb)
+        base = m.mla_sparse_decode_plan(4, heads, 2048)
+        assert not p["tensor_memory"]
+        assert {k: p[k] for k in base} == base
+    assert lib.mla_sparse_decode_plan_fmt(2, 4, 64, 2048, packed, 10, None, None, None, None) == 1  # unknown fmt
+    assert lib.mla_sparse_decode_plan_fmt(0, 4, 8, 2048, packed, 10, None, None, None, None) == 1
+
+
 def test_workspace_sizes_are_zero_for_empty_or_invalid(lib):
     assert lib.mla_sparse_decode_workspace_size(0, 16, 2048) == 0
     assert lib.mla_sparse_decode_workspace_size(4, 8, 2048) == 0
