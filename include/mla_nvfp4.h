@@ -231,6 +231,9 @@ mla_status_t mla_sparse_decode(const uint16_t* q_nope, const uint16_t* q_rope, c
  *  - The first call on a device looks up that device's address of the array
  *    (with the device current) and caches it; make that first call before any
  *    stream capture.  The call itself never calls cudaMalloc or cudaFree.
+ *    The cached address does not survive cudaDeviceReset (the array may be
+ *    placed elsewhere when the library's module is loaded again): a process
+ *    that resets a device must not call this entry point on it afterwards.
  *  - Every call on a device shares the same array, which keeps whatever the
  *    last call left there (nothing in it needs to start at zero).  Calls that
  *    overlap on the GPU -- on different streams, or from different host

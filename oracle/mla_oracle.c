@@ -28,7 +28,7 @@
  *  448) and OCP Microscaling Formats (MX) v1.0 (FP4 E2M1: values 0, 0.5, 1,
  *  1.5, 2, 3, 4, 6 and a sign bit).
  *
- * Readings where the pages are silent (all listed in the design doc as well):
+ * Readings where the pages are silent (the CUDA path implements the same ones):
  *  R-layout   NVFP4 row = [0,256) packed e2m1 codes, element 2i in the LOW
  *             nibble of byte i; [256,288) 32 e4m3 scales, scale g covering
  *             latent elements [16g,16g+16); [288,352) 64 rope values e4m3.

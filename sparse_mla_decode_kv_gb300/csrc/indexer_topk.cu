@@ -687,16 +687,10 @@ cudaError_t launch_topk(const float* scores, int64_t row_stride, const int32_t* 
   uint32_t* cand_key = static_cast<uint32_t*>(workspace);
   int32_t* cand_idx = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + lists);
   int32_t* cand_cnt = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + 2 * lists);
-  static int configured_device = -1;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<uint64_t> configured{0};
+  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(topk_kernel),
+                                      static_cast<int>(sizeof(TopkSmem)), &configured);
   if (e != cudaSuccess) return e;
-  if (configured_device != dev) {
-    e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(sizeof(TopkSmem)));
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
   topk_collect_kernel<<<dim3(kParts, batch), kPartThreads, 0, stream>>>(scores, row_stride, context_lens, topk,
                                                                        max_context_len, cand_key, cand_idx, cand_cnt);
   e = cudaGetLastError();
@@ -709,16 +703,10 @@ cudaError_t launch_topk(const float* scores, int64_t row_stride, const int32_t* 
 template <int NT>
 cudaError_t launch_idx_tma(const IdxArgs& a, const CUtensorMap& map, unsigned int* fw, dim3 grid, size_t smem,
                            cudaStream_t stream) {
-  static int configured_device = -1;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<uint64_t> configured{0};
+  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(indexer_scores_tma_kernel<NT>),
+                                      static_cast<int>(smem), &configured);
   if (e != cudaSuccess) return e;
-  if (configured_device != dev) {
-    e = cudaFuncSetAttribute(indexer_scores_tma_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
   indexer_scores_tma_kernel<NT><<<grid, kIdxWarps * 32, smem, stream>>>(a, map, fw);
   return cudaGetLastError();
 }

@@ -1,6 +1,7 @@
 // The C ABI of libmla_nvfp4.so (declared in include/mla_nvfp4.h): host-side
 // argument validation, workspace sizing and kernel dispatch.  Nothing here
 // allocates device memory; every launch goes to the caller's stream.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -87,32 +88,59 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 }  // namespace
 
+namespace {
+// Per-device caches of the SM count and the fault word's device address.
+// Host threads may drive different devices at once: each device has its own
+// slot (an atomic, so the fast path takes no lock), filled once under a
+// mutex.  A device index past the table is looked up on every call.
+constexpr int kMaxCachedDevices = 64;
+std::mutex g_cache_mutex;
+std::atomic<int> g_sm_count[kMaxCachedDevices];
+std::atomic<unsigned int*> g_fault_word_ptr[kMaxCachedDevices];
+
+int query_sm_count(int dev) {
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 148;
+  return sms;
+}
+unsigned int* query_fault_word() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_fault_word) != cudaSuccess) return nullptr;
+  return static_cast<unsigned int*>(p);
+}
+}  // namespace
+
 int device_sm_count() {
-  static int cached_dev = -1;
-  static int cached_sms = 0;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-  if (dev != cached_dev) {
-    int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 148;
-    cached_sms = sms;
-    cached_dev = dev;
+  if (dev < 0 || dev >= kMaxCachedDevices) return query_sm_count(dev);
+  int sms = g_sm_count[dev].load(std::memory_order_acquire);
+  if (sms > 0) return sms;
+  std::lock_guard<std::mutex> lock(g_cache_mutex);
+  sms = g_sm_count[dev].load(std::memory_order_relaxed);
+  if (sms <= 0) {
+    sms = query_sm_count(dev);
+    g_sm_count[dev].store(sms, std::memory_order_release);
   }
-  return cached_sms;
+  return sms;
 }
 
+// The address is cached per device for the life of the process; after a
+// cudaDeviceReset the library's device variables may move, so a process that
+// resets a device must not call into the library on it again.
 unsigned int* fault_word_ptr() {
-  static int cached_dev = -1;
-  static unsigned int* cached = nullptr;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-  if (dev != cached_dev) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_fault_word) != cudaSuccess) return nullptr;
-    cached = static_cast<unsigned int*>(p);
-    cached_dev = dev;
+  if (dev < 0 || dev >= kMaxCachedDevices) return query_fault_word();
+  unsigned int* p = g_fault_word_ptr[dev].load(std::memory_order_acquire);
+  if (p != nullptr) return p;
+  std::lock_guard<std::mutex> lock(g_cache_mutex);
+  p = g_fault_word_ptr[dev].load(std::memory_order_relaxed);
+  if (p == nullptr) {
+    p = query_fault_word();
+    if (p != nullptr) g_fault_word_ptr[dev].store(p, std::memory_order_release);
   }
-  return cached;
+  return p;
 }
 
 namespace {
@@ -135,6 +163,19 @@ EncodeTiledFn encode_tiled() {
   return fn;
 }
 }  // namespace
+
+bool tensor_maps_available() { return encode_tiled() != nullptr; }
+
+cudaError_t set_smem_limit_once(const void* kernel, int bytes, std::atomic<uint64_t>* done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t{1} << dev) : 0;
+  if (bit != 0 && (done->load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0) done->fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, uint64_t inner,
                           uint64_t rows, uint64_t row_stride, uint32_t box_inner, uint32_t box_rows,

@@ -106,6 +106,33 @@ __device__ __forceinline__ float lg2(float x) {
   return y;
 }
 
+// ---- query range --------------------------------------------------------------
+// The absorbed query arrives as bf16 (8 exponent bits) but feeds FP16
+// operands (5 exponent bits): a head whose values lie beyond +-65504 would
+// saturate and values below 2^-14 would lose bits.  Each head is therefore
+// scaled by a power of two 2^k that brings its largest magnitude into
+// [2^14, 2^15), and the head's softmax scale is multiplied by 2^-k: the
+// scaled scores are exactly the unscaled ones (powers of two are exact).
+//
+// Largest magnitude of the two bf16 values in `two`, as the 15 bits of the
+// magnitude (ordered like the values for every finite input).
+__device__ __forceinline__ uint32_t bf16x2_absmax_bits(uint32_t two) {
+  return max(two & 0x7FFFu, (two >> 16) & 0x7FFFu);
+}
+__device__ __forceinline__ uint32_t bf16x8_absmax_bits(uint4 v) {
+  return max(max(bf16x2_absmax_bits(v.x), bf16x2_absmax_bits(v.y)),
+             max(bf16x2_absmax_bits(v.z), bf16x2_absmax_bits(v.w)));
+}
+// The shift k for a head whose largest bf16 magnitude has bits `m`: 0 for an
+// all-zero head, else 14 - exponent, clamped so that 2^k and 2^-k are normal
+// floats (a subnormal maximum counts as exponent -127).
+__device__ __forceinline__ int query_shift(uint32_t m) {
+  if (m == 0) return 0;
+  const int e = static_cast<int>(m >> 7) - 127;
+  return min(126, max(-113, 14 - e));
+}
+__device__ __forceinline__ float pow2f(int k) { return __int_as_float((127 + k) << 23); }
+
 // ---- warp-level tensor core (m16n8k16, f16 x f16 -> f32) -------------------
 __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm(

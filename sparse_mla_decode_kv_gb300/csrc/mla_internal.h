@@ -2,6 +2,7 @@
 // kernel translation units.  Not part of the public interface.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
@@ -13,6 +14,12 @@ namespace mla {
 int device_sm_count();
 // Device address of the library's fault word on the current device.
 unsigned int* fault_word_ptr();
+// Raises a kernel's dynamic shared-memory limit to `bytes` once per device:
+// bit d of `*done` records device d (devices past 63 are configured on every
+// call).  Safe when host threads drive different devices at once.
+cudaError_t set_smem_limit_once(const void* kernel, int bytes, std::atomic<uint64_t>* done);
+// True when the driver's tensor-map encoder is available (TMA paths need it).
+bool tensor_maps_available();
 // A 2-D TMA tensor map (no interleave, zero fill out of bounds) over `rows`
 // rows of `inner` elements, rows `row_stride` bytes apart; box
 // {box_inner, box_rows}.  False when the driver entry point is unavailable

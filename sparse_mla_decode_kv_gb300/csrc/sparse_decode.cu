@@ -107,6 +107,7 @@ struct alignas(128) Smem {
   float alpha[kHeadsPerCta];
   int rescale[kConsumerWarps];
   float mfin[kHeadsPerCta];
+  uint32_t qmax[kConsumerWarps][kHeadsPerCta];  // per warp and head: largest |q| (bf16 magnitude bits)
   float lfin[kHeadsPerCta];
   int64_t row_off[kMaxRows];  // per row of the slice: byte offset in the pool (TMA: row index), -1 if masked
   int32_t tok_all[kMaxRows];  // token of each row of the slice, -1 if masked
@@ -147,8 +148,10 @@ __device__ __forceinline__ float2 half2_floats(uint32_t bits) {
   return __half22float2(*reinterpret_cast<const __half2*>(&bits));
 }
 
-__device__ __forceinline__ uint32_t bf16pair_to_f16x2(uint32_t two) {
-  return f32x2_to_f16x2_sat(bf16_bits_to_f32(two & 0xFFFFu), bf16_bits_to_f32(two >> 16));
+// Two bf16 query values times 2^k (`mul`) to f16x2; exact for every value
+// that lands in f16's normal range.
+__device__ __forceinline__ uint32_t bf16pair_to_f16x2(uint32_t two, float mul) {
+  return f32x2_to_f16x2_sat(bf16_bits_to_f32(two & 0xFFFFu) * mul, bf16_bits_to_f32(two >> 16) * mul);
 }
 
 // Cluster merge: the splits of one (request, head group) are the CTAs of a
@@ -316,7 +319,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  __syncthreads();  // barrier init and the resolved rows are visible
+  // Largest |q| of heads h0 and h0 + 8 over this warp's dims (the four lanes
+  // of a row group hold disjoint dims), for the per-head power-of-two shift.
+  {
+    uint32_t m0 = max(bf16x2_absmax_bits(qr_0.x), bf16x2_absmax_bits(qr_0.y));
+    uint32_t m1 = max(bf16x2_absmax_bits(qr_1.x), bf16x2_absmax_bits(qr_1.y));
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      m0 = max(m0, bf16x8_absmax_bits(qv0[q]));
+      m1 = max(m1, bf16x8_absmax_bits(qv1[q]));
+    }
+#pragma unroll
+    for (int off = 1; off < 4; off <<= 1) {
+      m0 = max(m0, __shfl_xor_sync(0xFFFFFFFFu, m0, off));
+      m1 = max(m1, __shfl_xor_sync(0xFFFFFFFFu, m1, off));
+    }
+    if (c == 0) {
+      sm.qmax[w][g] = m0;
+      sm.qmax[w][g + 8] = m1;
+    }
+  }
+  __syncthreads();  // barrier init, the resolved rows and the query maxima are visible
 
   // Fill stage `it` into its ring slot; masked rows arrive as zeros.
   // TMA: lane 0 of every warp posts its share of the stage's bytes on
@@ -355,17 +378,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   int next_fill = 0;
   for (; next_fill < min(n_stages, kInitialStages); ++next_fill) fill_stage(next_fill);
 
+  // Per-head shift k (largest |q| into [2^14, 2^15)): heads h0 and h0 + 8 for
+  // the fragments, heads 4w .. 4w + 3 (softmax owner) for the scale 2^-k.
+  auto head_shift = [&](int h) {
+    return query_shift(max(max(sm.qmax[0][h], sm.qmax[1][h]), max(sm.qmax[2][h], sm.qmax[3][h])));
+  };
+  const float qmul0 = pow2f(head_shift(g));
+  const float qmul1 = pow2f(head_shift(g + 8));
+  float scale_h[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) scale_h[e] = args.scale_log2 * pow2f(-head_shift(4 * w + e));
+
   // Stage the query as B fragments (K = this warp's 144 dims in the permuted
   // order, N = 16 heads) in fragment order: one 16-byte load per k-step.
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    sm.qfrag[w][2 * q][lane] = make_uint4(bf16pair_to_f16x2(qv0[q].x), bf16pair_to_f16x2(qv0[q].y),
-                                          bf16pair_to_f16x2(qv1[q].x), bf16pair_to_f16x2(qv1[q].y));
-    sm.qfrag[w][2 * q + 1][lane] = make_uint4(bf16pair_to_f16x2(qv0[q].z), bf16pair_to_f16x2(qv0[q].w),
-                                              bf16pair_to_f16x2(qv1[q].z), bf16pair_to_f16x2(qv1[q].w));
+    sm.qfrag[w][2 * q][lane] = make_uint4(bf16pair_to_f16x2(qv0[q].x, qmul0), bf16pair_to_f16x2(qv0[q].y, qmul0),
+                                          bf16pair_to_f16x2(qv1[q].x, qmul1), bf16pair_to_f16x2(qv1[q].y, qmul1));
+    sm.qfrag[w][2 * q + 1][lane] =
+        make_uint4(bf16pair_to_f16x2(qv0[q].z, qmul0), bf16pair_to_f16x2(qv0[q].w, qmul0),
+                   bf16pair_to_f16x2(qv1[q].z, qmul1), bf16pair_to_f16x2(qv1[q].w, qmul1));
   }
-  sm.qfrag[w][8][lane] = make_uint4(bf16pair_to_f16x2(qr_0.x), bf16pair_to_f16x2(qr_0.y),
-                                    bf16pair_to_f16x2(qr_1.x), bf16pair_to_f16x2(qr_1.y));
+  sm.qfrag[w][8][lane] = make_uint4(bf16pair_to_f16x2(qr_0.x, qmul0), bf16pair_to_f16x2(qr_0.y, qmul0),
+                                    bf16pair_to_f16x2(qr_1.x, qmul1), bf16pair_to_f16x2(qr_1.y, qmul1));
   __syncwarp();
 
   // -------------------------------------------------------------- consumers
@@ -518,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool need = false;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        z[e] = valid ? z[e] * args.scale_log2 : -INFINITY;
+        z[e] = valid ? z[e] * scale_h[e] : -INFINITY;
         need |= z[e] > m_ref[e] + kLazy;
       }
       float alpha[4] = {1.f, 1.f, 1.f, 1.f};
@@ -742,16 +777,10 @@ bool make_row_tensor_map(CUtensorMap* map, const void* pool, int64_t block_strid
 template <int FMT, bool TMA>
 cudaError_t launch_variant(const DecodeArgs& a, const CUtensorMap& map, int pairs, cudaStream_t stream) {
   const size_t smem = sizeof(Smem<FMT, TMA>);
-  static int configured_device = -1;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<uint64_t> configured{0};
+  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(sparse_decode_kernel<FMT, TMA>),
+                                      static_cast<int>(smem), &configured);
   if (e != cudaSuccess) return e;
-  if (configured_device != dev) {
-    e = cudaFuncSetAttribute(sparse_decode_kernel<FMT, TMA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pairs * a.splits * (a.num_heads / kHeadsPerCta));
   cfg.blockDim = dim3(kThreads);

@@ -17,7 +17,8 @@
 
 namespace {
 
-// Split-K partials (per request-head: 512 floats per split plus one LSE).
+// Split-K partials: per request-head and split, 512 f16 values of the
+// normalised partial output plus one float log-sum-exp.
 // Every GPU that loads the library holds this array until the process exits.
 constexpr size_t kScratchBytes = MLA_SPARSE_DECODE_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
@@ -27,7 +28,8 @@ std::mutex g_setup_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
 
 // The array's name is only a host-side stand-in: its device address has to be
-// looked up once per device, with that device current.
+// looked up once per device, with that device current.  The cache is not
+// invalidated by cudaDeviceReset; the header says so.
 mla_status_t scratch_for_current_device(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -86,9 +86,12 @@ struct alignas(1024) TcSmem {
   uint8_t chunk[kTcChunkBufs][kTcChunkBytes];  // unpacked operand chunks
   uint8_t p_op[kTcPBytes];               // P, MN-major: (h/8)*2048 + (r/8)*128 + (r%8)*16 + (h%8)*2
   int32_t tok[2][kTcRows];               // token of each row of the slot's stage, -1 if masked
-  float red[kTcUnpackWarps][32];         // per-warp, per-head reduction scratch
+  // per-warp, per-head reduction scratch of the softmax; before the first
+  // stage, its first 64 words hold each head's largest |q| (bf16 magnitude bits)
+  float red[kTcUnpackWarps][32];
   float m_ref[2][32];                    // running (lazy) maximum per head, base 2, per head half
   float alpha[2][32];                    // rescale factor of the last raise, per head half
+  float qscale[kTcHeads];                // per head: softmax scale (base 2) x 2^-shift of its query
   uint64_t raw_full[2], raw_free[2], chunk_full[kTcChunkBufs], chunk_free[kTcChunkBufs], s_full, p_full, done;
   uint32_t tmem_base;
   int abort_flag;
@@ -187,8 +190,9 @@ __device__ __forceinline__ bool tc_wait(TcSmem& sm, uint64_t* bar, uint32_t pari
   return false;
 }
 
-__device__ __forceinline__ uint32_t tc_bf16pair_to_f16x2(uint32_t two) {
-  return f32x2_to_f16x2_sat(bf16_bits_to_f32(two & 0xFFFFu), bf16_bits_to_f32(two >> 16));
+// Two bf16 query values times 2^k (`mul`) to f16x2.
+__device__ __forceinline__ uint32_t tc_bf16pair_to_f16x2(uint32_t two, float mul) {
+  return f32x2_to_f16x2_sat(bf16_bits_to_f32(two & 0xFFFFu) * mul, bf16_bits_to_f32(two >> 16) * mul);
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -225,6 +229,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(&sm.done, 1);
     sm.abort_flag = 0;
     for (int j = 0; j < 64; ++j) sm.m_ref[j >> 5][j & 31] = -INFINITY;
+    for (int j = 0; j < kTcHeads; ++j) reinterpret_cast<uint32_t*>(&sm.red[0][0])[j] = 0;
     fence_mbar_init();
   }
   if (warp == kTcUnpackWarps + 1) {
@@ -354,14 +359,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     ? __ldg(reinterpret_cast<const uint4*>(args.q_nope + (qrow + h) * kLatent) + dg)
                     : __ldg(reinterpret_cast<const uint4*>(args.q_rope + (qrow + h) * kRope) + (dg - kLatent / 8));
       }
+      // Per-head power-of-two shift bringing the largest |q| into
+      // [2^14, 2^15) (FP16 operands), undone in the head's softmax scale.
+      uint32_t* qmax = reinterpret_cast<uint32_t*>(&sm.red[0][0]);
+#pragma unroll
+      for (int i = 0; i < kQPer; ++i) {
+        const int u = threadIdx.x + i * kTcUnpackThreads;
+        atomicMax(&qmax[u / kDimGroups], bf16x8_absmax_bits(xs[i]));
+      }
+      named_bar_sync(1, kTcUnpackThreads);
+      if (threadIdx.x < kTcHeads)
+        sm.qscale[threadIdx.x] = args.scale_log2 * pow2f(-query_shift(qmax[threadIdx.x]));
 #pragma unroll
       for (int i = 0; i < kQPer; ++i) {
         const int u = threadIdx.x + i * kTcUnpackThreads;
         const int h = u / kDimGroups;
         const int dg = u - h * kDimGroups;
+        const float mul = pow2f(query_shift(qmax[h]));
         *reinterpret_cast<uint4*>(sm.q_op + (h >> 3) * kTcQHeadGroupBytes + dg * 128 + (h & 7) * 16) =
-            make_uint4(tc_bf16pair_to_f16x2(xs[i].x), tc_bf16pair_to_f16x2(xs[i].y),
-                       tc_bf16pair_to_f16x2(xs[i].z), tc_bf16pair_to_f16x2(xs[i].w));
+            make_uint4(tc_bf16pair_to_f16x2(xs[i].x, mul), tc_bf16pair_to_f16x2(xs[i].y, mul),
+                       tc_bf16pair_to_f16x2(xs[i].z, mul), tc_bf16pair_to_f16x2(xs[i].w, mul));
       }
       fence_async_smem();
     }
@@ -431,7 +448,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bool need = false;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        z[j] = valid ? __uint_as_float(sr[j]) * args.scale_log2 : -INFINITY;
+        z[j] = valid ? __uint_as_float(sr[j]) * sm.qscale[32 * half + j] : -INFINITY;
         need |= z[j] > m_ref[j] + kTcLazy;
       }
       bool rescale = false;
@@ -599,11 +616,12 @@ bool sparse_decode_tc_supported(int fmt, int num_heads) {
 }
 
 // The same conditions as the dispatch in launch_sparse_decode: the format
-// and head count, and a pool the row tensor map can describe (a stride of
-// whole rows, at least one block, row coordinates within 32 bits).
+// and head count, a pool the row tensor map can describe (a stride of whole
+// rows, at least one block, row coordinates within 32 bits) and a driver
+// that can encode tensor maps.
 bool sparse_decode_uses_tc(int fmt, int num_heads, int64_t block_stride, int64_t num_blocks) {
   if (!sparse_decode_tc_supported(fmt, num_heads) || num_blocks <= 0 || block_stride % kRowNvfp4 != 0) return false;
-  return num_blocks * (block_stride / kRowNvfp4) <= 0x7FFFFFFF;
+  return num_blocks * (block_stride / kRowNvfp4) <= 0x7FFFFFFF && tensor_maps_available();
 }
 
 int plan_sparse_decode_tc(int pairs, int num_heads, int topk, int max_splits) {
@@ -616,16 +634,10 @@ int plan_sparse_decode_tc(int pairs, int num_heads, int topk, int max_splits) {
 
 cudaError_t launch_sparse_decode_tc(const TcDecodeParams& p, const CUtensorMap& map, cudaStream_t stream) {
   const size_t smem = sizeof(TcSmem);
-  static int configured_device = -1;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<uint64_t> configured{0};
+  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(sparse_decode_tc_kernel),
+                                      static_cast<int>(smem), &configured);
   if (e != cudaSuccess) return e;
-  if (configured_device != dev) {
-    e = cudaFuncSetAttribute(sparse_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
   TcArgs a;
   a.q_nope = p.q_nope;
   a.q_rope = p.q_rope;

@@ -146,10 +146,20 @@ def test_decode_plan_for_format_and_pool(lib):
     import sparse_mla_decode_kv_gb300 as m
     nvfp4, fp8 = 0, 1
     packed = 64 * 352
+    # The kernel also needs the driver's tensor-map encoder: without a driver
+    # (a build box) the plan is the 16-head one, as the dispatch would be.
+    try:
+        C.CDLL("libcuda.so.1")
+        driver = True
+    except OSError:
+        driver = False
     for batch, heads, topk in [(128, 64, 2048), (1, 64, 2048), (2, 128, 700), (6, 64, 2048), (3, 64, 1)]:
         p = m.mla_sparse_decode_plan_fmt(nvfp4, batch, heads, topk, packed, 1000)
         base = m.mla_sparse_decode_plan(batch, heads, topk)
-        assert p["tensor_memory"]
+        assert p["tensor_memory"] == driver
+        if not driver:
+            assert {k: p[k] for k in base} == base
+            continue
         assert 1 <= p["splits"] <= base["splits"]
         assert p["splits"] * p["rows_per_split"] >= topk and (p["splits"] - 1) * p["rows_per_split"] < topk
         assert p["kernels"] == (2 if p["splits"] > 1 else 1)
@@ -207,3 +217,18 @@ def test_staged_path_validation_and_sizes(lib):
     bad = list(base)
     bad[3] = 64 * 352 - 16  # stride too small for 352-byte rows
     assert g(*bad) == 1
+
+
+def test_no_alloc_decode_rejects_scratch_beyond_its_array(lib):
+    """mla_sparse_decode_noalloc keeps its split-K scratch in a fixed 16 MiB
+    array: a shape whose scratch exceeds it is refused with
+    MLA_ERR_WORKSPACE_TOO_SMALL before any device lookup or launch, so the
+    call is safe to make on a machine without a GPU."""
+    cap = 16 << 20
+    f = lib.mla_sparse_decode_noalloc
+    for batch, heads in [(128, 128), (512, 16), (128, 64)]:
+        need = lib.mla_sparse_decode_workspace_size(batch, heads, 2048)
+        assert need > cap, (batch, heads, need)
+        assert f(FAKE, FAKE, FAKE, 64 * 352, 10, FAKE, 4, FAKE, FAKE, batch, heads, 64, 2048, 0.07, FAKE, None,
+                 None) == 3
+    assert 0 < lib.mla_sparse_decode_workspace_size(32, 16, 2048) <= cap  # the TP4 rank fits

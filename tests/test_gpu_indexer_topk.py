@@ -157,14 +157,16 @@ def test_chained_indexer_topk_decode_full_size():
                                  dec.block_table, dec.context_lens, dec.topk_idx, dec.softmax_scale, lse=lse)
     torch.cuda.synchronize()
     out, lse = out.float().cpu().numpy(), lse.cpu().numpy()
+    # the oracle decodes the rows the GPU selected (whatever near-tie swaps
+    # the top-k made), so every sampled request is checked
     for b in [0, 21, 42, 63]:
-        sel = torch.from_numpy(O.topk(ref[b], 2048).astype(np.int64)).to(DEV)
+        got = idx[b][idx[b] >= 0].astype(np.int64)
+        sel = torch.from_numpy(got).to(DEV)
         lat, rope = dec.request_rows(b, sel)
-        valid = np.ones(2048, bool)
+        valid = np.ones(got.size, bool)
         r, rl = oracle_rows_decode(u16(dec.q_nope[b]), u16(dec.q_rope[b]), u16(lat), u16(rope), valid, 0,
                                    dec.softmax_scale)
-        if set(idx[b].tolist()) == set(O.topk(ref[b], 2048).tolist()):
-            assert_decode_close(out[b], lse[b], r, rl, f"request {b}")
+        assert_decode_close(out[b], lse[b], r, rl, f"request {b}")
 
 
 def test_indexer_key_stride_not_a_multiple_of_128():
