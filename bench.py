@@ -54,7 +54,10 @@ def parse():
     p.add_argument("--append-sessions", type=int, default=64, help="sessions in the quantize-on-write sub-benchmark")
     p.add_argument("--indexer-batch", type=int, default=64, help="requests in the indexer + top-k sub-benchmark")
     p.add_argument("--only-extras", action="store_true", help="time only the sub-benchmarks (profiling)")
-    p.add_argument("--draft-tokens", type=int, default=4, help="query tokens per request in the draft-token timing")
+    p.add_argument("--draft-tokens", type=str, default="4,15",
+                   help="query tokens per request in the draft-token timings (comma-separated; the pages' "
+                        "native kernel decodes 15 per launch)")
+    p.add_argument("--no-chain", action="store_true", help="skip the chained indexer + top-k + decode timing")
     p.add_argument("--no-dep", action="store_true", help="skip the 128 x 64-head (DEP rank) decode timing")
     p.add_argument("--dep-tokens", type=int, default=24_000_000,
                    help="cached tokens of the DEP rank in total (a smaller pool, same 128 x 2,048 selected rows)")
@@ -72,10 +75,12 @@ def peaks():
 
 
 # DRAM traffic of one NVFP4 decode launch of the TP4-rank workload
-# (dram__bytes_read.sum + dram__bytes_write.sum from one ncu capture of 65,536
-# selected rows; profiles/sparse_decode_nvfp4_tp4_rank.md), and a digest of
-# the kernel source it was taken on: once the source differs, the figure no
-# longer describes the kernel and is reported as null.
+# (dram__bytes_read.sum + dram__bytes_write.sum from one ncu capture of one
+# launch over 65,536 selected rows, `ncu --metrics dram__bytes_read.sum,
+# dram__bytes_write.sum --clock-control none -k regex:sparse_decode_kernel
+# -s 1 -c 1` on `bench.py --ctx 16384 --layers 2 --no-extras`), and a digest
+# of the kernel source it was taken on: once the source differs, the figure
+# no longer describes the kernel and is reported as null.
 E2E_CHUNKS = 4  # copy chunks per step of the end-to-end pass
 DECODE_NVFP4_TRAFFIC = {"bytes": 29_491_968 + 2_304, "source_digest": "4ad1549542e4635a"}
 KERNEL_SOURCES = ("sparse_mla_decode_kv_gb300/csrc/sparse_decode.cu", "sparse_mla_decode_kv_gb300/csrc/mla_device.cuh")
@@ -350,35 +355,58 @@ def main():
         layers.append(wl)
     ws_bytes = m.mla_sparse_decode_workspace_size(B, H, K)
     workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
-    # the staged path's FP8 copy is a temporary buffer that every layer reuses
-    ws_staged = torch.empty(m.mla_sparse_decode_staged_workspace_size(B, H, K), dtype=torch.uint8, device=dev)
+    # The staged path: every layer gets its own FP8 copy (576-byte rows, with
+    # the identity block table and list the copy kernel writes beside it), and
+    # a step first stages all L layers, then runs the L FP8 decodes on the
+    # copies.  The L copies together are far larger than L2, so the copy is
+    # written to and read back from HBM, as on the pages.
+    nblk_st = (K + 63) // 64
+    st_pool_bytes = m.mla_staged_pool_bytes(B, K)
+    staged = [{"pool": torch.empty(st_pool_bytes, dtype=torch.uint8, device=dev),
+               "list": torch.empty((B, K), dtype=torch.int32, device=dev)} for _ in range(L)]
+    st_table = torch.arange(B * nblk_st, dtype=torch.int32, device=dev).view(B, nblk_st)
+    st_ctx = torch.full((B,), nblk_st * 64, dtype=torch.int32, device=dev)
     torch.cuda.synchronize()
 
     stream = torch.cuda.Stream(device=dev)
 
     def decode_all(fmt):
-        # fmt 0: native NVFP4, 1: FP8 cache, 2: staged NVFP4 (gather to an FP8 copy, then the FP8 decode)
-        fn = {0: m.mla_sparse_decode, 1: m.mla_sparse_decode_fp8, 2: m.mla_sparse_decode_staged}[fmt]
-        pool_fmt = 1 if fmt == 1 else 0
-        ws = ws_staged if fmt == 2 else workspace
+        # fmt 0: native NVFP4, 1: FP8 cache
+        fn = {0: m.mla_sparse_decode, 1: m.mla_sparse_decode_fp8}[fmt]
         for wl in layers:
-            fn(wl.q_nope, wl.q_rope, wl.pools[pool_fmt], wl.strides[pool_fmt], wl.num_blocks, wl.block_table,
-               wl.context_lens, wl.topk_idx, wl.softmax_scale, out=wl.out, lse=wl.lse, workspace=ws,
+            fn(wl.q_nope, wl.q_rope, wl.pools[fmt], wl.strides[fmt], wl.num_blocks, wl.block_table,
+               wl.context_lens, wl.topk_idx, wl.softmax_scale, out=wl.out, lse=wl.lse, workspace=workspace,
                stream=stream)
 
-    # Draft tokens: Q query tokens per request, each with its own top-k list
-    # (90% shared with its neighbours), over the same layer caches.
-    Q = args.draft_tokens
-    drafts = [W.draft_queries(wl, q_len=Q) for wl in layers]
-    ws_mtp = torch.empty(max(m.mla_sparse_decode_mtp_workspace_size(B, Q, H, K), 256), dtype=torch.uint8, device=dev)
-    out_mtp = torch.empty((B, Q, H, 512), dtype=torch.bfloat16, device=dev)
-    lse_mtp = torch.empty((B, Q, H), dtype=torch.float32, device=dev)
+    def staged_all():
+        # staged NVFP4: gather every layer's selected rows into its FP8 copy, then decode the copies
+        for wl, st in zip(layers, staged):
+            m.mla_stage_rows_fp8(wl.pools[0], wl.strides[0], wl.num_blocks, wl.block_table, wl.context_lens,
+                                 wl.topk_idx, staged_pool=st["pool"], staged_topk=st["list"], stream=stream)
+        for wl, st in zip(layers, staged):
+            m.mla_sparse_decode_fp8(wl.q_nope, wl.q_rope, st["pool"], 64 * ROW_FP8, B * nblk_st, st_table, st_ctx,
+                                    st["list"], wl.softmax_scale, out=wl.out, lse=wl.lse, workspace=workspace,
+                                    stream=stream)
 
-    def drafts_all():
-        for wl, dq in zip(layers, drafts):
+    # Draft tokens: Q query tokens per request, each with its own top-k list
+    # (90% shared with its neighbours), over the same layer caches; one
+    # timing per Q (4, and the pages' 15 per launch).
+    draft_qs = [int(x) for x in args.draft_tokens.split(",") if x.strip()]
+    draft_sets = {}
+    for Q in draft_qs:
+        draft_sets[Q] = {
+            "drafts": [W.draft_queries(wl, q_len=Q) for wl in layers],
+            "ws": torch.empty(max(m.mla_sparse_decode_mtp_workspace_size(B, Q, H, K), 256), dtype=torch.uint8,
+                              device=dev),
+            "out": torch.empty((B, Q, H, 512), dtype=torch.bfloat16, device=dev),
+            "lse": torch.empty((B, Q, H), dtype=torch.float32, device=dev)}
+
+    def drafts_all(Q):
+        d = draft_sets[Q]
+        for wl, dq in zip(layers, d["drafts"]):
             m.mla_sparse_decode_mtp(dq.q_nope, dq.q_rope, wl.pools[0], wl.strides[0], wl.num_blocks, wl.block_table,
-                                    wl.context_lens, dq.topk_idx, wl.softmax_scale, out=out_mtp, lse=lse_mtp,
-                                    workspace=ws_mtp, stream=stream)
+                                    wl.context_lens, dq.topk_idx, wl.softmax_scale, out=d["out"], lse=d["lse"],
+                                    workspace=d["ws"], stream=stream)
 
     def capture(fn):
         g = torch.cuda.CUDAGraph()
@@ -389,8 +417,9 @@ def main():
                 fn()
         return g
 
-    graphs = {0: capture(lambda: decode_all(0)), 1: capture(lambda: decode_all(1)), 2: capture(lambda: decode_all(2)),
-              3: capture(drafts_all)}
+    graphs = {0: capture(lambda: decode_all(0)), 1: capture(lambda: decode_all(1)), 2: capture(staged_all)}
+    for Q in draft_qs:
+        graphs[("mtp", Q)] = capture(lambda Q=Q: drafts_all(Q))
     torch.cuda.synchronize()
 
     def timed(g, steps, warmup):
@@ -417,7 +446,7 @@ def main():
         ms4 = timed(graphs[0], args.steps, args.warmup)
         ms8 = timed(graphs[1], args.steps, args.warmup)
         ms_st = timed(graphs[2], args.steps, args.warmup)
-        ms_mtp = timed(graphs[3], args.steps, args.warmup)
+        ms_mtp = {Q: timed(graphs[("mtp", Q)], args.steps, args.warmup) for Q in draft_qs}
     clk = clocks.summary()
     plan = m.mla_sparse_decode_plan(B, H, K)
     launches_per_step = L * plan["kernels"]
@@ -425,9 +454,18 @@ def main():
     per_layer4 = ms4 / L * 1e-3
     per_layer8 = ms8 / L * 1e-3
     per_layer_st = ms_st / L * 1e-3
-    per_layer_mtp = ms_mtp / L * 1e-3
-    # rows a layer must read at least once: distinct valid entries over a request's Q lists (layer 0)
-    distinct = sum(int(torch.unique(drafts[0].topk_idx[b][drafts[0].topk_idx[b] >= 0]).numel()) for b in range(B))
+
+    def draft_entry(Q):
+        per_layer = ms_mtp[Q] / L * 1e-3
+        dq0 = draft_sets[Q]["drafts"][0]
+        # rows a layer must read at least once: distinct valid entries over a request's Q lists (layer 0)
+        distinct = sum(int(torch.unique(dq0.topk_idx[b][dq0.topk_idx[b] >= 0]).numel()) for b in range(B))
+        return {"q_len": Q, "value": whole_job_rate(B * Q * K, world, per_layer), "unit": UNIT,
+                "per_layer_us": per_layer * 1e6, "vs_single_token": per_layer / per_layer4,
+                "distinct_rows_per_layer": distinct,
+                "hbm_gbs_distinct_rows": (distinct * (ROW_NVFP4 + 4) + B * Q * H * 2180) / per_layer / 1e9,
+                "note": f"{Q} query tokens per request, each with its own top-2048 list (90% shared), one "
+                        "launch per layer"}
     rows = B * K
     value = whole_job_rate(rows, world, per_layer4)
     ach4 = layer_bytes4 / per_layer4 / 1e9
@@ -559,15 +597,11 @@ def main():
         "staged": {"value": whole_job_rate(rows, world, per_layer_st), "unit": UNIT,
                    "per_layer_us": per_layer_st * 1e6, "vs_native": per_layer_st / per_layer4,
                    "vs_fp8": per_layer_st / per_layer8,
-                   "bytes_per_row": ROW_NVFP4 + 4 + 2 * (ROW_FP8 + 4),
-                   "note": "gather kernel writes a 576-byte FP8 copy of each selected row into a buffer every "
-                           "layer reuses, then the FP8 decode reads it"},
-        "drafts": {"q_len": Q, "value": whole_job_rate(B * Q * K, world, per_layer_mtp), "unit": UNIT,
-                   "per_layer_us": per_layer_mtp * 1e6, "vs_single_token": per_layer_mtp / per_layer4,
-                   "distinct_rows_per_layer": distinct,
-                   "hbm_gbs_distinct_rows": (distinct * (ROW_NVFP4 + 4) + B * Q * H * 2180) / per_layer_mtp / 1e9,
-                   "note": f"{Q} query tokens per request, each with its own top-2048 list (90% shared), one "
-                           "launch per layer"},
+                   "algorithmic_bytes_per_row": ROW_NVFP4 + 4 + 2 * (ROW_FP8 + 4),
+                   "note": f"a step gathers every layer's selected rows into its own 576-byte FP8 copy "
+                           f"({L} copies of {st_pool_bytes / 1e6:.1f} MB, far beyond L2), then runs the {L} FP8 "
+                           "decodes on the copies"},
+        "drafts": [draft_entry(Q) for Q in draft_qs],
         "nvfp4_bytes_per_row": ROW_NVFP4 + 4,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
@@ -656,11 +690,70 @@ def sub_measurements(m, W, dev, stream, args, hbm):
     key_bytes = tokens * 132
     out["indexer_topk"] = {"workload": iw.name, "us": t * 1e6, "tokens_per_s": tokens / t,
                            "key_hbm_gbs": key_bytes / t / 1e9, "frac": key_bytes / t / 1e9 / hbm}
+    if not args.no_chain:
+        out["chain"] = chain_measurement(m, W, dev, stream, args, hbm, iw, ws, tk)
     del iw, ws
     torch.cuda.empty_cache()
     if not args.no_dep:
         out["dep_rank"] = dep_measurement(m, W, dev, stream, args, hbm)
     return out
+
+
+def chain_measurement(m, W, dev, stream, args, hbm, iw, ws, tk):
+    """The whole path of one decode step and layer: the indexer scores every
+    cached token of the 64 requests (140,000 each), keeps the exact top-2048,
+    and the NVFP4 sparse decode of 16 MLA heads reads those rows -- the two
+    calls captured in one CUDA graph and timed together."""
+    import torch
+    _, tf_burst, _, _ = peaks()
+    nb = iw.q_idx.shape[0]
+    kv = W.tp4_rank_decode(dev, seed=77, batch=nb, ctx=140_000)
+
+    def qa(lat, rope, slots, pool, n_blocks, stride, fmt):
+        m.mla_kv_quantize_append(lat, rope, slots, pool, n_blocks, 64, stride, fmt)
+
+    W.fill_pool(kv, 0, qa)
+    H, K = kv.heads, 2048
+    dws = torch.empty(max(m.mla_sparse_decode_workspace_size(nb, H, K), 256), dtype=torch.uint8, device=dev)
+    out_t = torch.empty((nb, H, 512), dtype=torch.bfloat16, device=dev)
+    lse_t = torch.empty((nb, H), dtype=torch.float32, device=dev)
+    max_ctx = 140_000
+
+    def chain():
+        m.mla_indexer_topk(iw.q_idx, iw.head_w, iw.key_pool, iw.key_stride, iw.num_blocks, iw.block_table,
+                           iw.context_lens, K, max_ctx, topk_out=tk, workspace=ws, stream=stream)
+        m.mla_sparse_decode(kv.q_nope, kv.q_rope, kv.pools[0], kv.strides[0], kv.num_blocks, kv.block_table,
+                            kv.context_lens, tk, kv.softmax_scale, out=out_t, lse=lse_t, workspace=dws, stream=stream)
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        chain()
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            chain()
+        for _ in range(args.warmup):
+            g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    t = e0.elapsed_time(e1) / args.steps * 1e-3
+    tokens = nb * max_ctx
+    idx_bytes = tokens * 132 + nb * 32 * (128 * 2 + 4) + nb * K * 4
+    dec_bytes = decode_bytes(nb, H, K, ROW_NVFP4)
+    flops = tokens * 32 * 128 * 2 + decode_flops(nb, H, K)
+    roof = max((idx_bytes + dec_bytes) / (hbm * 1e9), flops / (tf_burst * 1e12))
+    res = {"workload": f"{nb} requests x {max_ctx:,} tokens: indexer (32 heads x 128, e4m3 keys) + exact "
+                       f"top-{K} + NVFP4 sparse decode of {H} heads on the selected rows, one CUDA graph",
+           "us": t * 1e6, "algorithmic_bytes": idx_bytes + dec_bytes, "hbm_gbs": (idx_bytes + dec_bytes) / t / 1e9,
+           "roofline_us": roof * 1e6, "frac_of_roofline_time": roof / t,
+           "note": "the float32 score row of every request (35.8 MB in all) is scratch between the indexer and the "
+                   "top-k and is not counted"}
+    del kv, dws
+    torch.cuda.empty_cache()
+    return res
 
 
 def dep_measurement(m, W, dev, stream, args, hbm):
@@ -715,8 +808,8 @@ def dep_measurement(m, W, dev, stream, args, hbm):
 
 
 def cpu_baseline(m, W, dev):
-    """The float64 oracle on a bounded sample of the same workload (4 requests
-    of one layer), on all host cores."""
+    """The float64 oracle on a bounded sample of the same workload (one layer's
+    32 requests), timed on all host cores and single-threaded."""
     import numpy as np
     import torch
     import oracle as O
@@ -738,16 +831,24 @@ def cpu_baseline(m, W, dev):
     bt = np.arange(len(reqs) * nblk, dtype=np.int32).reshape(len(reqs), nblk)
     idx = np.tile(np.arange(K, dtype=np.int32), (len(reqs), 1))
     cl = np.full(len(reqs), K, np.int32)
-    # Repeat whole-layer decodes until about 10 s of CPU time (threads x wall) is spent.
-    reps, t_total = 0, 0.0
-    while reps < 20 and t_total * threads < 10.0:
-        t0 = time.perf_counter()
-        O.sparse_decode(qn, qr, pool, 64 * ROW_NVFP4, bt, cl, idx, 64, wl.softmax_scale, 0, threads=threads)
-        t_total += time.perf_counter() - t0
-        reps += 1
-    return {"value": reps * len(reqs) * K / t_total, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{reps} x one layer ({len(reqs)} requests x {K} rows of 352 B), float64, "
-                      f"{t_total:.2f} s wall on {threads} threads"}
+    # Median of 3 timed runs, on all host cores (one layer: 32 requests) and
+    # single-threaded (8 of the 32 requests, to stay bounded).
+    def median_rate(n_req, n_threads):
+        times = []
+        for _ in range(3):
+            t0 = time.perf_counter()
+            O.sparse_decode(qn[:n_req], qr[:n_req], pool, 64 * ROW_NVFP4, bt[:n_req], cl[:n_req], idx[:n_req], 64,
+                            wl.softmax_scale, 0, threads=n_threads)
+            times.append(time.perf_counter() - t0)
+        return n_req * K / statistics.median(times), statistics.median(times)
+
+    all_rate, all_t = median_rate(len(reqs), threads)
+    one_rate, one_t = median_rate(8, 1)
+    return {"value": all_rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"one layer ({len(reqs)} requests x {K} rows of 352 B), float64, median of 3 runs "
+                      f"({all_t:.3f} s each) on {threads} threads",
+            "single_thread": {"value": one_rate, "unit": UNIT, "cores": 1,
+                              "sample": f"8 requests x {K} rows, float64, median of 3 runs ({one_t:.3f} s each)"}}
 
 
 if __name__ == "__main__":
