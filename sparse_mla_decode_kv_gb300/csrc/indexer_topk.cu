@@ -27,6 +27,8 @@
 // the whole row instead.
 #include <cuda_fp16.h>
 
+#include <algorithm>
+
 #include "mla_device.cuh"
 #include "mla_internal.h"
 
@@ -54,6 +56,7 @@ struct IdxArgs {
   int max_blocks;
   int n_heads;
   int max_ctx;
+  int batch;
 };
 
 // Row address of token t's key (nullptr when masked) and its scale.
@@ -305,6 +308,231 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 3)
       if (t0 < ctx) out_row[t0] = p0;
       if (t1 < ctx) out_row[t1] = p1;
     }
+  }
+}
+
+// Pipelined variant (TMA, up to 32 index heads): a persistent grid of two
+// CTAs per SM, each walking a contiguous range of 256-token chunks (request
+// major, so the query changes rarely).  A producer warp resolves each
+// chunk's four block ids (eight chunks per batch of lookups, one lane per
+// block) and loads its keys (64 x 128-byte TMA tiles, 128-byte swizzle) and
+// scales (256-byte bulk copies) into a three-slot ring, up to three chunks
+// ahead; four compute warps take row group w of every block, two 16-token
+// tiles at a time so that eight accumulator chains are in flight, and hand
+// the slot back.  Compared with one CTA per 512 tokens, no chunk waits for
+// its own block-table lookups and copies: they were issued while the
+// previous chunks were multiplied.
+constexpr int kPipeChunk = 256;                  // tokens per chunk
+constexpr int kPipeBlocks = kPipeChunk / kBlock;  // 4 key blocks
+constexpr int kPipeSlots = 3;
+constexpr int kPipeComputeWarps = 4;
+constexpr int kPipeThreads = (kPipeComputeWarps + 1) * 32;
+constexpr uint32_t kPipeBlockBytes = kIdxBlockBytesKeys + kBlock * 4;  // 8,448 bytes per block
+
+struct alignas(1024) IdxPipeSmem {
+  uint8_t keys[kPipeSlots][kPipeBlocks][kBlock][kIdxDim];  // 8 KB per block (1024-byte aligned)
+  float scales[kPipeSlots][kPipeBlocks][kBlock];
+  int32_t pblk[kPipeSlots][kPipeBlocks];  // physical block; -1: outside the pool (-inf); -2: past the context
+  uint64_t full[kPipeSlots];
+  uint64_t empty[kPipeSlots];
+  int abort_flag;
+};
+
+template <int NT>  // n-tiles of 8 heads
+__global__ void __launch_bounds__(kPipeThreads, 2)
+    indexer_scores_pipe_kernel(const IdxArgs a, const __grid_constant__ CUtensorMap tmap, unsigned int* fault_word) {
+  extern __shared__ uint8_t idx_smem_raw[];
+  IdxPipeSmem& sm =
+      *reinterpret_cast<IdxPipeSmem*>(idx_smem_raw + ((1024u - (smem_u32(idx_smem_raw) & 1023u)) & 1023u));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_chunk = (a.max_ctx + kPipeChunk - 1) / kPipeChunk;
+  const int64_t n_items = static_cast<int64_t>(a.batch) * n_chunk;
+  const int64_t per = (n_items + gridDim.x - 1) / gridDim.x;
+  const int64_t it_begin = static_cast<int64_t>(blockIdx.x) * per;
+  const int64_t it_end = min(n_items, it_begin + per);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kPipeSlots; ++i) {
+      mbar_init(&sm.full[i], 1);
+      mbar_init(&sm.empty[i], kPipeComputeWarps);
+    }
+    sm.abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kPipeComputeWarps) {
+    // ------------------------------------------------------------ producer
+    const int64_t rows_per_block = a.block_stride / kIdxDim;
+    int s = 0;
+    bool stop = false;
+    for (int64_t base = it_begin; base < it_end && !stop; base += 8) {
+      // lane l: block l % 4 of item base + l / 4
+      const int64_t item = base + lane / 4;
+      int pb = -2;
+      bool live = false;
+      if (item < it_end) {
+        const int b = static_cast<int>(item / n_chunk);
+        const int chunk = static_cast<int>(item - static_cast<int64_t>(b) * n_chunk);
+        const int ctx = min(__ldg(a.ctx_lens + b), a.max_ctx);
+        live = chunk * kPipeChunk < ctx;
+        const int lb = chunk * kPipeBlocks + (lane & 3);
+        if (lb * kBlock < ctx) {
+          pb = -1;
+          if (lb < a.max_blocks) {
+            const int p = __ldg(a.block_table + static_cast<int64_t>(b) * a.max_blocks + lb);
+            if (p >= 0 && p < a.num_blocks) pb = p;
+          }
+        }
+      }
+      const uint32_t live_mask = __ballot_sync(0xFFFFFFFFu, live);
+      const uint32_t valid_mask = __ballot_sync(0xFFFFFFFFu, pb >= 0);
+      for (int k = 0; k < 8; ++k) {
+        if (!((live_mask >> (4 * k)) & 1u)) continue;  // empty item (past the context): nothing to load
+        const int slot = s % kPipeSlots;
+        bool ok = true;
+        if (lane == 0 && s >= kPipeSlots)
+          ok = mbar_wait_or_abort(&sm.empty[slot], static_cast<uint32_t>(s / kPipeSlots - 1) & 1u, &sm.abort_flag,
+                                  fault_word, kFaultIndexerWait);
+        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
+          if (lane == 0) sm.abort_flag = 1;
+          stop = true;
+          break;
+        }
+        const bool mine = (lane >> 2) == k;
+        if (mine) sm.pblk[slot][lane & 3] = pb;
+        __syncwarp();
+        if (lane == 0)
+          mbar_expect_tx(&sm.full[slot], __popc((valid_mask >> (4 * k)) & 0xFu) * kPipeBlockBytes);
+        __syncwarp();
+        if (mine && pb >= 0) {
+          tma_load_2d(sm.keys[slot][lane & 3][0], &tmap, 0, static_cast<int>(pb * rows_per_block), &sm.full[slot]);
+          bulk_load(sm.scales[slot][lane & 3], a.pool + static_cast<int64_t>(pb) * a.block_stride + kIdxBlockBytesKeys,
+                    kBlock * 4, &sm.full[slot]);
+        }
+        ++s;
+      }
+    }
+    // no copy may be in flight when the CTA exits
+    if (lane == 0)
+      for (int j = max(0, s - kPipeSlots); j < s; ++j)
+        mbar_wait_bounded(&sm.full[j % kPipeSlots], static_cast<uint32_t>(j / kPipeSlots) & 1u, fault_word,
+                          kFaultIndexerWait);
+    return;
+  }
+
+  // ------------------------------------------------------------ compute warps
+  const int g = lane >> 2, c = lane & 3;
+  uint32_t bq[8][NT][2];
+  float wh[NT][2];
+  int cur_b = -1, ctx = 0;
+  int s = 0;
+  for (int64_t item = it_begin; item < it_end; ++item) {
+    const int b = static_cast<int>(item / n_chunk);
+    const int chunk = static_cast<int>(item - static_cast<int64_t>(b) * n_chunk);
+    if (b != cur_b) {
+      // the request's query (B fragments, K permuted like the keys) and head weights
+      cur_b = b;
+      ctx = min(__ldg(a.ctx_lens + b), a.max_ctx);
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        const uint16_t* qh = a.q + (static_cast<int64_t>(b) * a.n_heads + 8 * n + g) * kIdxDim;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(qh + 32 * q + 8 * c));
+          bq[2 * q][n][0] = bf16pair_to_f16x2(v.x);
+          bq[2 * q][n][1] = bf16pair_to_f16x2(v.y);
+          bq[2 * q + 1][n][0] = bf16pair_to_f16x2(v.z);
+          bq[2 * q + 1][n][1] = bf16pair_to_f16x2(v.w);
+        }
+        const float* wb = a.w + static_cast<int64_t>(b) * a.n_heads;
+        wh[n][0] = __ldg(wb + 8 * n + 2 * c);
+        wh[n][1] = __ldg(wb + 8 * n + 2 * c + 1);
+      }
+    }
+    if (chunk * kPipeChunk >= ctx) continue;
+    const int slot = s % kPipeSlots;
+    const bool ok = mbar_wait_or_abort(&sm.full[slot], static_cast<uint32_t>(s / kPipeSlots) & 1u, &sm.abort_flag,
+                                       fault_word, kFaultIndexerWait);
+    if (!__all_sync(0xFFFFFFFFu, ok)) {
+      if (lane == 0) sm.abort_flag = 1;
+      break;
+    }
+    float* out_row = a.scores + static_cast<int64_t>(b) * a.scores_stride;
+    const int t_base = chunk * kPipeChunk;
+#pragma unroll 1
+    for (int p = 0; p < 2; ++p) {
+      // tiles (row group `warp` of blocks 2p and 2p + 1)
+      const int blk0 = 2 * p, blk1 = 2 * p + 1;
+      const int r0 = 16 * warp + g;  // tile rows r0 and r0 + 8; (r & 7) == g
+      const int pb0 = sm.pblk[slot][blk0], pb1 = sm.pblk[slot][blk1];
+      float acc0[NT][4], acc1[NT][4];
+#pragma unroll
+      for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc0[n][e] = acc1[n][e] = 0.f;
+      const uint8_t* k00 = sm.keys[slot][blk0][r0];
+      const uint8_t* k01 = sm.keys[slot][blk0][r0 + 8];
+      const uint8_t* k10 = sm.keys[slot][blk1][r0];
+      const uint8_t* k11 = sm.keys[slot][blk1][r0 + 8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int off = (((2 * q + (c >> 1)) ^ g) << 4) + 8 * (c & 1);
+        const uint2 u00 = *reinterpret_cast<const uint2*>(k00 + off);
+        const uint2 u01 = *reinterpret_cast<const uint2*>(k01 + off);
+        const uint2 u10 = *reinterpret_cast<const uint2*>(k10 + off);
+        const uint2 u11 = *reinterpret_cast<const uint2*>(k11 + off);
+        uint32_t x00[2], x01[2], y00[2], y01[2], x10[2], x11[2], y10[2], y11[2];
+        e4m3x4_to_f16x2x2(u00.x, x00);
+        e4m3x4_to_f16x2x2(u01.x, x01);
+        e4m3x4_to_f16x2x2(u00.y, y00);
+        e4m3x4_to_f16x2x2(u01.y, y01);
+        e4m3x4_to_f16x2x2(u10.x, x10);
+        e4m3x4_to_f16x2x2(u11.x, x11);
+        e4m3x4_to_f16x2x2(u10.y, y10);
+        e4m3x4_to_f16x2x2(u11.y, y11);
+        const uint32_t A00[4] = {x00[0], x01[0], x00[1], x01[1]};
+        const uint32_t A01[4] = {y00[0], y01[0], y00[1], y01[1]};
+        const uint32_t A10[4] = {x10[0], x11[0], x10[1], x11[1]};
+        const uint32_t A11[4] = {y10[0], y11[0], y10[1], y11[1]};
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          mma_f16(acc0[n], A00, bq[2 * q][n][0], bq[2 * q][n][1]);
+          mma_f16(acc1[n], A10, bq[2 * q][n][0], bq[2 * q][n][1]);
+        }
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          mma_f16(acc0[n], A01, bq[2 * q + 1][n][0], bq[2 * q + 1][n][1]);
+          mma_f16(acc1[n], A11, bq[2 * q + 1][n][0], bq[2 * q + 1][n][1]);
+        }
+      }
+      // sum_h w_h * relu(s_t * dot): this lane holds heads 8n + 2c + {0,1}
+#pragma unroll
+      for (int tt = 0; tt < 2; ++tt) {
+        const int blk = tt ? blk1 : blk0;
+        const int pbk = tt ? pb1 : pb0;
+        const float(&acc)[NT][4] = tt ? acc1 : acc0;
+        const float s0 = sm.scales[slot][blk][r0];
+        const float s1 = sm.scales[slot][blk][r0 + 8];
+        float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          p0 += wh[n][0] * fmaxf(s0 * acc[n][0], 0.f) + wh[n][1] * fmaxf(s0 * acc[n][1], 0.f);
+          p1 += wh[n][0] * fmaxf(s1 * acc[n][2], 0.f) + wh[n][1] * fmaxf(s1 * acc[n][3], 0.f);
+        }
+        p0 += __shfl_xor_sync(0xFFFFFFFFu, p0, 1);
+        p0 += __shfl_xor_sync(0xFFFFFFFFu, p0, 2);
+        p1 += __shfl_xor_sync(0xFFFFFFFFu, p1, 1);
+        p1 += __shfl_xor_sync(0xFFFFFFFFu, p1, 2);
+        const int t0 = t_base + blk * kBlock + r0;
+        if (c == 0 && pbk != -2) {  // -2: the whole block lies past the context
+          if (t0 < ctx) out_row[t0] = pbk >= 0 ? p0 : -INFINITY;
+          if (t0 + 8 < ctx) out_row[t0 + 8] = pbk >= 0 ? p1 : -INFINITY;
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[slot]);
+    ++s;
   }
 }
 
@@ -701,6 +929,19 @@ cudaError_t launch_topk(const float* scores, int64_t row_stride, const int32_t* 
 }
 
 template <int NT>
+cudaError_t launch_idx_pipe(const IdxArgs& a, const CUtensorMap& map, unsigned int* fw, cudaStream_t stream) {
+  const size_t smem = sizeof(IdxPipeSmem) + 1024;
+  static std::atomic<uint64_t> configured{0};
+  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(indexer_scores_pipe_kernel<NT>),
+                                      static_cast<int>(smem), &configured);
+  if (e != cudaSuccess) return e;
+  const int64_t n_items = static_cast<int64_t>(a.batch) * ((a.max_ctx + kPipeChunk - 1) / kPipeChunk);
+  const int64_t grid = std::min<int64_t>(n_items, 2 * static_cast<int64_t>(device_sm_count()));
+  indexer_scores_pipe_kernel<NT><<<static_cast<unsigned>(grid), kPipeThreads, smem, stream>>>(a, map, fw);
+  return cudaGetLastError();
+}
+
+template <int NT>
 cudaError_t launch_idx_tma(const IdxArgs& a, const CUtensorMap& map, unsigned int* fw, dim3 grid, size_t smem,
                            cudaStream_t stream) {
   static std::atomic<uint64_t> configured{0};
@@ -729,6 +970,7 @@ cudaError_t launch_indexer_scores(const uint16_t* q_idx, const float* head_w, co
   a.max_blocks = max_blocks_per_req;
   a.n_heads = n_heads;
   a.max_ctx = max_context_len;
+  a.batch = batch;
   dim3 grid((max_context_len + kIdxTokensPerCta - 1) / kIdxTokensPerCta, batch);
   CUtensorMap map;
   const int64_t rows = num_blocks * (block_stride / kIdxDim);
@@ -738,9 +980,9 @@ cudaError_t launch_indexer_scores(const uint16_t* q_idx, const float* head_w, co
                            CU_TENSOR_MAP_SWIZZLE_128B)) {
     const size_t smem = sizeof(IdxSmem) + 1024;
     switch (n_heads / 8) {
-      case 1: return launch_idx_tma<1>(a, map, fw, grid, smem, stream);
-      case 2: return launch_idx_tma<2>(a, map, fw, grid, smem, stream);
-      case 4: return launch_idx_tma<4>(a, map, fw, grid, smem, stream);
+      case 1: return launch_idx_pipe<1>(a, map, fw, stream);
+      case 2: return launch_idx_pipe<2>(a, map, fw, stream);
+      case 4: return launch_idx_pipe<4>(a, map, fw, stream);
       case 8: return launch_idx_tma<8>(a, map, fw, grid, smem, stream);
       default: return cudaErrorInvalidValue;
     }

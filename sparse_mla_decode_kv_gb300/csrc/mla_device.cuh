@@ -208,6 +208,26 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   atomicOr(fault_word, fault);
   return false;
 }
+// The same bounded wait, but it also gives up (returning false, without
+// setting a fault bit) as soon as another warp of the CTA has set
+// *abort_flag -- that warp timed out, and the phase may never complete.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, const int* abort_flag,
+                                                   unsigned int* fault_word, unsigned int fault) {
+  const volatile int* flag = abort_flag;
+  for (uint32_t i = 0; i < kSpinPolls; ++i) {
+    if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+    if (*flag) return false;
+  }
+  uint32_t ns = 64;
+  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+    __nanosleep(ns);
+    if (ns < 1024) ns <<= 1;
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*flag) return false;
+  }
+  atomicOr(fault_word, fault);
+  return false;
+}
 // 16-byte global -> shared copy (cp.async, L2 only).  With src_bytes == 0
 // nothing is read and the 16 destination bytes are zero-filled.
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src, uint32_t src_bytes) {
