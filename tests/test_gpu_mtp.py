@@ -95,15 +95,17 @@ def test_single_token_equals_plain_decode():
     assert torch.equal(a[:, 0], b)
 
 
-def test_tp4_rank_drafts_full_size_sampled():
-    """32 requests x 4 tokens x 16 heads, 140,000-token contexts, per-token
-    top-2048 lists overlapping 90% (as bench.py times); 2 requests x 4 tokens
-    checked against the oracle on the rows each token selects."""
+@pytest.mark.parametrize("q_len,tokens", [(4, [0, 1, 2, 3]), (15, [0, 7, 14])])
+def test_tp4_rank_drafts_full_size_sampled(q_len, tokens):
+    """32 requests x q_len tokens x 16 heads, 140,000-token contexts,
+    per-token top-2048 lists overlapping 90% (as bench.py times, at 4 tokens
+    and at the pages' 15 per launch); 2 requests x a few tokens checked
+    against the oracle on the rows each token selects."""
     m = lib()
     wl = W.tp4_rank_decode(DEV)
-    dq = W.draft_queries(wl, q_len=4)
+    dq = W.draft_queries(wl, q_len=q_len)
     W.fill_pool(wl, O.FMT_NVFP4, quantize_fn(m))
-    lse = torch.empty((32, 4, 16), dtype=torch.float32, device=DEV)
+    lse = torch.empty((32, q_len, 16), dtype=torch.float32, device=DEV)
     out, _ = m.mla_sparse_decode_mtp(dq.q_nope, dq.q_rope, wl.pools[0], wl.strides[0], wl.num_blocks,
                                      wl.block_table, wl.context_lens, dq.topk_idx, wl.softmax_scale, lse=lse)
     torch.cuda.synchronize()
@@ -111,9 +113,9 @@ def test_tp4_rank_drafts_full_size_sampled():
     assert np.isfinite(out).all() and np.isfinite(lse).all()
     for b in [5, 30]:
         c = int(wl.context_lens[b])
-        for i in range(4):
+        for i in tokens:
             idx = dq.topk_idx[b, i].cpu().numpy().astype(np.int64)
-            valid = (idx >= 0) & (idx < c - (4 - 1 - i))
+            valid = (idx >= 0) & (idx < c - (q_len - 1 - i))
             lat, rope = wl.request_rows(b, torch.from_numpy(np.where(valid, idx, 0)).to(DEV))
             ref, ref_lse = oracle_rows_decode(u16(dq.q_nope[b, i]), u16(dq.q_rope[b, i]), u16(lat), u16(rope), valid,
                                               O.FMT_NVFP4, wl.softmax_scale)
