@@ -5,13 +5,19 @@
 // indexer key is 128 e4m3 bytes and a float scale.  The score
 // is sum_h w_h * relu(s_t * (q_h . k_t)).
 //
-// indexer_scores_kernel: one CTA = 4 warps over 512 tokens of one request.
-// Each warp takes 16-token m-tiles; the keys are loaded straight from the
-// paged pool (8 bytes per lane per 32-dim chunk, prefetched one m-tile
-// ahead), converted e4m3x2 -> f16x2 into mma.sync A fragments and multiplied
-// by the n_heads query rows held as B fragments; the epilogue applies the
-// per-token scale, relu and head weights and reduces over heads with two
-// shuffles.  HBM-bound at 132 bytes per token.
+// Three score kernels, by the key pool's stride and the number of heads:
+//  * indexer_scores_tc_kernel (key blocks TMA can tile, 32 or 64 heads): a
+//    persistent grid; a producer warp loads 128-token chunks of key tiles
+//    into a ring, the products run on the tcgen05 tensor cores with e4m3
+//    operands (keys as stored, the query split into two e4m3 parts) and
+//    accumulators in tensor memory, and four warps apply relu, the token
+//    scale and the head weights, one token per thread.
+//  * indexer_scores_pipe_kernel (TMA-tileable pools, 8 or 16 heads): the
+//    same persistent ring, products on mma.sync with the query in registers.
+//  * indexer_scores_kernel (other strides): one CTA = 4 warps over 512 tokens
+//    of one request, keys loaded straight from the paged pool one m-tile
+//    ahead, mma.sync.
+// All are HBM-bound at 132 bytes per token.
 //
 // Top-k in two kernels.  Scores map to order-preserving 32-bit keys (with
 // -0.0 folded into +0.0).  topk_collect_kernel: 8 CTAs per request each draw
@@ -173,141 +179,6 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 3) indexer_scores_kernel(const
     s1 = ns1;
     ok0 = nok0;
     ok1 = nok1;
-  }
-}
-
-// TMA variant (the pool's block stride is a multiple of 128 bytes, so the key
-// pool is a 2-D tensor of 128-byte rows): the CTA's 8 key blocks (64 tokens
-// x 128 bytes each) land in shared memory as 8 tiles with the 128-byte
-// swizzle, their scales as 8 bulk copies of 256 bytes, all issued at entry
-// (66 KB in flight per CTA); each block has its own mbarrier so the warps
-// start on block 0 while the rest arrive.  The swizzle puts the 16-byte
-// chunk j of tile row r at chunk j ^ (r & 7), so the 8 rows a fragment load
-// touches hit 8 different bank groups.
-constexpr int kIdxBlocksPerCta = kIdxTokensPerCta / kBlock;  // 8
-
-struct alignas(1024) IdxSmem {
-  uint8_t keys[kIdxBlocksPerCta][kBlock][kIdxDim];  // 8 KB per block, 1024-byte aligned (swizzle atom)
-  float scales[kIdxBlocksPerCta][kBlock];
-  uint64_t bar[kIdxBlocksPerCta];
-  int32_t pblk[kIdxBlocksPerCta];  // physical block, -1 if invalid or past the context
-};
-
-template <int NT>  // n-tiles of 8 heads
-__global__ void __launch_bounds__(kIdxWarps * 32, 3)
-    indexer_scores_tma_kernel(const IdxArgs a, const __grid_constant__ CUtensorMap tmap, unsigned int* fault_word) {
-  extern __shared__ uint8_t idx_smem_raw[];
-  // The swizzled tiles need a 1024-byte aligned base.
-  IdxSmem& sm = *reinterpret_cast<IdxSmem*>(idx_smem_raw + ((1024u - (smem_u32(idx_smem_raw) & 1023u)) & 1023u));
-  const int b = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, c = lane & 3;
-  const int ctx = min(__ldg(a.ctx_lens + b), a.max_ctx);
-  const int t_begin = blockIdx.x * kIdxTokensPerCta;
-  if (t_begin >= ctx) return;
-  const int32_t* bt_row = a.block_table + static_cast<int64_t>(b) * a.max_blocks;
-  const int lb0 = t_begin / kBlock;
-
-  if (threadIdx.x < kIdxBlocksPerCta) {
-    const int lb = lb0 + threadIdx.x;
-    int pb = -1;
-    if (lb * kBlock < ctx && lb < a.max_blocks) {
-      pb = __ldg(bt_row + lb);
-      if (pb < 0 || pb >= a.num_blocks) pb = -1;
-    }
-    sm.pblk[threadIdx.x] = pb;
-    mbar_init(&sm.bar[threadIdx.x], 1);
-  }
-  fence_mbar_init();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const int64_t rows_per_block = a.block_stride / kIdxDim;
-#pragma unroll 1
-    for (int i = 0; i < kIdxBlocksPerCta; ++i) {
-      const int pb = sm.pblk[i];
-      if (pb < 0) continue;
-      mbar_expect_tx(&sm.bar[i], kIdxBlockBytesKeys + kBlock * 4);
-      tma_load_2d(sm.keys[i][0], &tmap, 0, static_cast<int>(pb * rows_per_block), &sm.bar[i]);
-      bulk_load(sm.scales[i], a.pool + static_cast<int64_t>(pb) * a.block_stride + kIdxBlockBytesKeys, kBlock * 4,
-                &sm.bar[i]);
-    }
-  }
-
-  // Query B fragments (K = 128 dims permuted like the keys, N = 8*NT heads) and head weights.
-  uint32_t bq[8][NT][2];
-  float wh[NT][2];
-#pragma unroll
-  for (int n = 0; n < NT; ++n) {
-    const int h = 8 * n + g;
-    const uint16_t* qh = a.q + (static_cast<int64_t>(b) * a.n_heads + h) * kIdxDim;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(qh + 32 * q + 8 * c));
-      bq[2 * q][n][0] = bf16pair_to_f16x2(v.x);
-      bq[2 * q][n][1] = bf16pair_to_f16x2(v.y);
-      bq[2 * q + 1][n][0] = bf16pair_to_f16x2(v.z);
-      bq[2 * q + 1][n][1] = bf16pair_to_f16x2(v.w);
-    }
-    const float* wb = a.w + static_cast<int64_t>(b) * a.n_heads;
-    wh[n][0] = __ldg(wb + 8 * n + 2 * c);
-    wh[n][1] = __ldg(wb + 8 * n + 2 * c + 1);
-  }
-
-  float* out_row = a.scores + static_cast<int64_t>(b) * a.scores_stride;
-  constexpr int kTiles = kIdxTokensPerCta / 16;
-  for (int mt = warp; mt < kTiles && t_begin + 16 * mt < ctx; mt += kIdxWarps) {
-    const int blk = mt / (kBlock / 16);
-    const int r0 = (mt % (kBlock / 16)) * 16 + g;  // tile rows r0 and r0 + 8; (r & 7) == g for both
-    const int t0 = t_begin + 16 * mt + g;
-    const int t1 = t0 + 8;
-    if (sm.pblk[blk] < 0) {  // block id outside the pool: the block's tokens score -inf
-      if (c == 0) {
-        if (t0 < ctx) out_row[t0] = -INFINITY;
-        if (t1 < ctx) out_row[t1] = -INFINITY;
-      }
-      continue;
-    }
-    if (!mbar_wait_bounded(&sm.bar[blk], 0u, fault_word, kFaultIndexerWait)) continue;
-    const uint8_t* row0 = sm.keys[blk][r0];
-    const uint8_t* row1 = sm.keys[blk][r0 + 8];
-    float acc[NT][4];
-#pragma unroll
-    for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int off = (((2 * q + (c >> 1)) ^ g) << 4) + 8 * (c & 1);
-      const uint2 v0 = *reinterpret_cast<const uint2*>(row0 + off);
-      const uint2 v1 = *reinterpret_cast<const uint2*>(row1 + off);
-      uint32_t x0[2], x1[2], y0[2], y1[2];
-      e4m3x4_to_f16x2x2(v0.x, x0);
-      e4m3x4_to_f16x2x2(v1.x, x1);
-      e4m3x4_to_f16x2x2(v0.y, y0);
-      e4m3x4_to_f16x2x2(v1.y, y1);
-      uint32_t A0[4] = {x0[0], x1[0], x0[1], x1[1]};
-      uint32_t A1[4] = {y0[0], y1[0], y0[1], y1[1]};
-#pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        mma_f16(acc[n], A0, bq[2 * q][n][0], bq[2 * q][n][1]);
-        mma_f16(acc[n], A1, bq[2 * q + 1][n][0], bq[2 * q + 1][n][1]);
-      }
-    }
-    const float s0 = sm.scales[blk][r0];
-    const float s1 = sm.scales[blk][r0 + 8];
-    // sum_h w_h * relu(s_t * dot): this lane holds heads 8n + 2c + {0,1}.
-    float p0 = 0.f, p1 = 0.f;
-#pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      p0 += wh[n][0] * fmaxf(s0 * acc[n][0], 0.f) + wh[n][1] * fmaxf(s0 * acc[n][1], 0.f);
-      p1 += wh[n][0] * fmaxf(s1 * acc[n][2], 0.f) + wh[n][1] * fmaxf(s1 * acc[n][3], 0.f);
-    }
-    p0 += __shfl_xor_sync(0xFFFFFFFFu, p0, 1);
-    p0 += __shfl_xor_sync(0xFFFFFFFFu, p0, 2);
-    p1 += __shfl_xor_sync(0xFFFFFFFFu, p1, 1);
-    p1 += __shfl_xor_sync(0xFFFFFFFFu, p1, 2);
-    if (c == 0) {
-      if (t0 < ctx) out_row[t0] = p0;
-      if (t1 < ctx) out_row[t1] = p1;
-    }
   }
 }
 
@@ -534,6 +405,292 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
     if (lane == 0) mbar_arrive(&sm.empty[slot]);
     ++s;
   }
+}
+
+// Tensor-memory variant (TMA key tiles, 32 or 64 index heads): the products
+// run on the fifth-generation tensor cores with 8-bit operands, the keys
+// straight from the TMA tiles.  The bf16 query of head h is scaled by a
+// power of two 2^k_h that brings its largest magnitude into [128, 256) and
+// split into two e4m3 parts, hi = e4m3(q 2^k_h) and lo = e4m3(q 2^k_h - hi):
+// a bf16 value has 8 significant bits and each part 4, so hi + lo is exact
+// for every element of at least 2^-2 (after scaling), and within 2^-10 (the
+// e4m3 subnormal step) for the smaller ones.  B = [hi rows; lo rows], N = 2
+// x heads, so one MMA chain gives both partial dot products of every head:
+// D[t, h] + D[t, H + h] = 2^k_h (q_h . k_t) for the 128 tokens t of a chunk
+// (M = 128, four K = 32 steps over the 128 dims).  Roles: warp 4 loads key
+// tiles and scales into a four-slot ring (as the pipelined kernel); warp 5
+// owns the tensor memory (two accumulators of N columns) and one of its
+// lanes issues the MMAs; warps 0-3 -- tensor-memory lanes 0-127, one token
+// each -- read the accumulator, apply relu, the token scale and the head
+// weights (times 2^-k_h), store the score, and write the split query when
+// the request changes.
+constexpr int kTcIdxChunk = 128;                    // tokens per chunk = MMA M
+constexpr int kTcIdxBlocks = kTcIdxChunk / kBlock;  // 2 key blocks
+constexpr int kTcIdxSlots = 4;
+constexpr int kTcIdxEpiWarps = 4;
+constexpr int kTcIdxThreads = (kTcIdxEpiWarps + 2) * 32;
+constexpr int kTcIdxItemsPerLookup = 32 / kTcIdxBlocks;
+
+template <int H>
+struct alignas(1024) TcIdxSmem {
+  uint8_t keys[kTcIdxSlots][kTcIdxBlocks][kBlock][kIdxDim];  // 16 KB per slot, 128-byte swizzle (TMA)
+  uint8_t qop[2 * H][kIdxDim];  // B operand: rows 0..H-1 hi parts, H..2H-1 lo parts, 128-byte swizzle
+  float scales[kTcIdxSlots][kTcIdxBlocks][kBlock];
+  float wq[H];  // w_h * 2^-k_h
+  int32_t pblk[kTcIdxSlots][kTcIdxBlocks];  // physical block; -1: outside the pool (-inf); -2: past the context
+  uint64_t raw_full[kTcIdxSlots], raw_empty[kTcIdxSlots], acc_full[2], acc_empty[2], b_ready;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int H>
+__global__ void __launch_bounds__(kTcIdxThreads, 2)
+    indexer_scores_tc_kernel(const IdxArgs a, const __grid_constant__ CUtensorMap tmap, unsigned int* fault_word) {
+  constexpr int N = 2 * H;                                  // accumulator columns per chunk
+  constexpr uint32_t kCols = 2 * N;                         // two accumulators
+  constexpr uint32_t kIdesc = umma_idesc_f32acc(kTcIdxChunk, N, 0, 0);  // e4m3 x e4m3 -> f32
+  static_assert(N % 16 == 0 && N <= 256 && (kCols & (kCols - 1)) == 0, "tensor-memory shape");
+  extern __shared__ uint8_t idx_smem_raw[];
+  TcIdxSmem<H>& sm =
+      *reinterpret_cast<TcIdxSmem<H>*>(idx_smem_raw + ((1024u - (smem_u32(idx_smem_raw) & 1023u)) & 1023u));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_chunk = (a.max_ctx + kTcIdxChunk - 1) / kTcIdxChunk;
+  const int64_t n_items = static_cast<int64_t>(a.batch) * n_chunk;
+  const int64_t per = (n_items + gridDim.x - 1) / gridDim.x;
+  const int64_t it_begin = static_cast<int64_t>(blockIdx.x) * per;
+  const int64_t it_end = min(n_items, it_begin + per);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kTcIdxSlots; ++i) {
+      mbar_init(&sm.raw_full[i], 1);
+      mbar_init(&sm.raw_empty[i], kTcIdxEpiWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.acc_full[i], 1);
+      mbar_init(&sm.acc_empty[i], kTcIdxEpiWarps);
+    }
+    mbar_init(&sm.b_ready, kTcIdxEpiWarps);
+    sm.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kTcIdxEpiWarps + 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sm.tmem_base)),
+                 "r"(kCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tcgen05_fence_before();
+  __syncthreads();
+  tcgen05_fence_after();
+  const uint32_t tbase = sm.tmem_base;
+  auto wait = [&](uint64_t* bar, uint32_t parity) {
+    const bool ok = mbar_wait_or_abort(bar, parity, &sm.abort_flag, fault_word, kFaultIndexerWait);
+    if (!ok) *reinterpret_cast<volatile int*>(&sm.abort_flag) = 1;
+    return ok;
+  };
+
+  if (warp == kTcIdxEpiWarps) {
+    // ------------------------------------------------------------ producer
+    const int64_t rows_per_block = a.block_stride / kIdxDim;
+    int s = 0;
+    bool stop = false;
+    for (int64_t base = it_begin; base < it_end && !stop; base += kTcIdxItemsPerLookup) {
+      const int64_t item = base + lane / kTcIdxBlocks;  // lane l: block l % 2 of item base + l / 2
+      int pb = -2;
+      bool live = false;
+      if (item < it_end) {
+        const int b = static_cast<int>(item / n_chunk);
+        const int chunk = static_cast<int>(item - static_cast<int64_t>(b) * n_chunk);
+        const int ctx = min(__ldg(a.ctx_lens + b), a.max_ctx);
+        live = chunk * kTcIdxChunk < ctx;
+        const int lb = chunk * kTcIdxBlocks + lane % kTcIdxBlocks;
+        if (lb * kBlock < ctx) {
+          pb = -1;
+          if (lb < a.max_blocks) {
+            const int p = __ldg(a.block_table + static_cast<int64_t>(b) * a.max_blocks + lb);
+            if (p >= 0 && p < a.num_blocks) pb = p;
+          }
+        }
+      }
+      const uint32_t live_mask = __ballot_sync(0xFFFFFFFFu, live);
+      const uint32_t valid_mask = __ballot_sync(0xFFFFFFFFu, pb >= 0);
+      for (int k = 0; k < kTcIdxItemsPerLookup; ++k) {
+        if (!((live_mask >> (kTcIdxBlocks * k)) & 1u)) continue;  // empty item (past the context)
+        const int slot = s % kTcIdxSlots;
+        bool ok = true;
+        if (lane == 0 && s >= kTcIdxSlots) ok = wait(&sm.raw_empty[slot], static_cast<uint32_t>(s / kTcIdxSlots - 1) & 1u);
+        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
+          stop = true;
+          break;
+        }
+        const bool mine = lane / kTcIdxBlocks == k;
+        const int j = lane % kTcIdxBlocks;
+        if (mine) sm.pblk[slot][j] = pb;
+        __syncwarp();
+        if (lane == 0)
+          mbar_expect_tx(&sm.raw_full[slot], __popc((valid_mask >> (kTcIdxBlocks * k)) & 3u) * (kIdxBlockBytesKeys + kBlock * 4));
+        __syncwarp();
+        if (mine && pb >= 0) {
+          tma_load_2d(sm.keys[slot][j][0], &tmap, 0, static_cast<int>(pb * rows_per_block), &sm.raw_full[slot]);
+          bulk_load(sm.scales[slot][j], a.pool + static_cast<int64_t>(pb) * a.block_stride + kIdxBlockBytesKeys,
+                    kBlock * 4, &sm.raw_full[slot]);
+        }
+        ++s;
+      }
+    }
+    // no copy may be in flight when the CTA leaves
+    if (lane == 0)
+      for (int j = max(0, s - kTcIdxSlots); j < s; ++j)
+        mbar_wait_bounded(&sm.raw_full[j % kTcIdxSlots], static_cast<uint32_t>(j / kTcIdxSlots) & 1u, fault_word,
+                          kFaultIndexerWait);
+  } else if (warp == kTcIdxEpiWarps + 1) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      const uint64_t b_desc = umma_desc_sw128(smem_u32(sm.qop));
+      int s = 0, cur_b = -1, cur_ctx_b = -1, ctx = 0, changes = 0;
+      for (int64_t item = it_begin; item < it_end; ++item) {
+        const int b = static_cast<int>(item / n_chunk);
+        const int chunk = static_cast<int>(item - static_cast<int64_t>(b) * n_chunk);
+        if (b != cur_ctx_b) {
+          cur_ctx_b = b;
+          ctx = min(__ldg(a.ctx_lens + b), a.max_ctx);
+        }
+        if (chunk * kTcIdxChunk >= ctx) continue;
+        if (b != cur_b) {  // the epilogue warps have written this request's split query
+          if (!wait(&sm.b_ready, static_cast<uint32_t>(changes) & 1u)) break;
+          ++changes;
+          cur_b = b;
+        }
+        const int slot = s % kTcIdxSlots, acc = s & 1;
+        if (!wait(&sm.raw_full[slot], static_cast<uint32_t>(s / kTcIdxSlots) & 1u)) break;
+        if (s >= 2 && !wait(&sm.acc_empty[acc], static_cast<uint32_t>(s / 2 - 1) & 1u)) break;
+        tcgen05_fence_after();
+        const uint64_t a_desc = umma_desc_sw128(smem_u32(sm.keys[slot][0][0]));
+#pragma unroll
+        for (int kk = 0; kk < kIdxDim / 32; ++kk)  // K = 32 e4m3 values = 32 bytes per step: +2 in the address field
+          umma_f8(tbase + static_cast<uint32_t>(acc * N), a_desc + 2 * kk, b_desc + 2 * kk, kIdesc, kk > 0);
+        umma_commit(&sm.acc_full[acc]);
+        ++s;
+      }
+      // every MMA issued above has completed once the last commit has arrived
+      if (s > 0)
+        mbar_wait_bounded(&sm.acc_full[(s - 1) & 1], static_cast<uint32_t>((s - 1) / 2) & 1u, fault_word,
+                          kFaultIndexerWait);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------- epilogue (warps 0-3)
+    const int t = threadIdx.x;  // token row of the chunk = tensor-memory lane
+    const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+    int s = 0, cur_b = -1, cur_ctx_b = -1, ctx = 0;
+    // After a timed-out wait the warp keeps walking its items without waiting
+    // or computing, so that every epilogue warp still meets the barriers of
+    // the query rewrites.
+    bool aborted = false;
+    for (int64_t item = it_begin; item < it_end; ++item) {
+      const int b = static_cast<int>(item / n_chunk);
+      const int chunk = static_cast<int>(item - static_cast<int64_t>(b) * n_chunk);
+      if (b != cur_ctx_b) {
+        cur_ctx_b = b;
+        ctx = min(__ldg(a.ctx_lens + b), a.max_ctx);
+      }
+      if (chunk * kTcIdxChunk >= ctx) continue;
+      if (b != cur_b) {
+        // The split query of request b.  Every MMA of earlier requests has
+        // completed (this warp waited for all their accumulators) and the MMA
+        // lane waits for b_ready before the next one, so B can be rewritten.
+        cur_b = b;
+        for (int u = t; u < H * 4; u += kTcIdxEpiWarps * 32) {
+          const int h = u >> 2, qd = u & 3;  // head h, dims 32 qd .. 32 qd + 31 (lanes 4g .. 4g+3 share h)
+          const uint4* qh = reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(b) * a.n_heads + h) * kIdxDim +
+                                                           32 * qd);
+          uint4 v[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) v[i] = __ldg(qh + i);
+          uint32_t m = max(max(bf16x8_absmax_bits(v[0]), bf16x8_absmax_bits(v[1])),
+                           max(bf16x8_absmax_bits(v[2]), bf16x8_absmax_bits(v[3])));
+          m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+          m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+          // largest |q| into [128, 256): k = 7 - exponent (a subnormal maximum counts as -127)
+          const int k = m == 0 ? 0 : min(126, max(-120, 7 - (static_cast<int>(m >> 7) - 127)));
+          const float mul = pow2f(k);
+          uint32_t hi[8], lo[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {  // four values -> one word of hi and one of lo
+              const float f0 = bf16_bits_to_f32(w4[2 * p] & 0xFFFFu) * mul;
+              const float f1 = bf16_bits_to_f32(w4[2 * p] >> 16) * mul;
+              const float f2 = bf16_bits_to_f32(w4[2 * p + 1] & 0xFFFFu) * mul;
+              const float f3 = bf16_bits_to_f32(w4[2 * p + 1] >> 16) * mul;
+              const uint32_t hw = f32x2_to_e4m3x2(f1, f0) | (f32x2_to_e4m3x2(f3, f2) << 16);
+              uint32_t back[2];
+              e4m3x4_to_f16x2x2(hw, back);
+              const float2 b01 = __half22float2(*reinterpret_cast<const __half2*>(&back[0]));
+              const float2 b23 = __half22float2(*reinterpret_cast<const __half2*>(&back[1]));
+              hi[2 * i + p] = hw;
+              lo[2 * i + p] = f32x2_to_e4m3x2(f1 - b01.y, f0 - b01.x) | (f32x2_to_e4m3x2(f3 - b23.y, f2 - b23.x) << 16);
+            }
+          }
+          // bytes 32 qd .. 32 qd + 31 of rows h (hi) and H + h (lo): 16-byte
+          // chunks 2 qd and 2 qd + 1, at chunk ^ (row % 8) (128-byte swizzle)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int ch = 2 * qd + c;
+            *reinterpret_cast<uint4*>(&sm.qop[h][(ch ^ (h & 7)) * 16]) =
+                make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
+            *reinterpret_cast<uint4*>(&sm.qop[H + h][(ch ^ ((H + h) & 7)) * 16]) =
+                make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
+          }
+          if (qd == 0) sm.wq[h] = __ldg(a.w + static_cast<int64_t>(b) * a.n_heads + h) * pow2f(-k);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.b_ready);
+        named_bar_sync(1, kTcIdxEpiWarps * 32);  // every head weight written before any epilogue reads it
+      }
+      if (aborted) continue;
+      const int slot = s % kTcIdxSlots, acc = s & 1;
+      bool ok = wait(&sm.acc_full[acc], static_cast<uint32_t>(s / 2) & 1u);
+      // the producer's block ids and scales of this slot (already complete)
+      ok = ok && wait(&sm.raw_full[slot], static_cast<uint32_t>(s / kTcIdxSlots) & 1u);
+      if (!__all_sync(0xFFFFFFFFu, ok)) {
+        aborted = true;
+        continue;
+      }
+      tcgen05_fence_after();
+      const int blk = t / kBlock, r = t % kBlock;
+      const float st = sm.scales[slot][blk][r];
+      float score = 0.f;
+#pragma unroll
+      for (int hg = 0; hg < H; hg += 32) {
+        uint32_t hv[32], lv[32];
+        tmem_load_32cols(tbase + lane_base + static_cast<uint32_t>(acc * N + hg), hv);
+        tmem_load_32cols(tbase + lane_base + static_cast<uint32_t>(acc * N + H + hg), lv);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          score += sm.wq[hg + j] * fmaxf(st * (__uint_as_float(hv[j]) + __uint_as_float(lv[j])), 0.f);
+      }
+      tcgen05_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.acc_empty[acc]);
+      const int pb = sm.pblk[slot][blk];
+      const int tok = chunk * kTcIdxChunk + t;
+      if (pb != -2 && tok < ctx)
+        a.scores[static_cast<int64_t>(b) * a.scores_stride + tok] = pb >= 0 ? score : -INFINITY;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.raw_empty[slot]);
+      ++s;
+    }
+  }
+
+  // ---- teardown: every copy and MMA has completed (the producer and the MMA
+  // lane waited for them); free the tensor memory
+  tcgen05_fence_before();
+  __syncthreads();
+  tcgen05_fence_after();
+  if (warp == kTcIdxEpiWarps + 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(kCols) : "memory");
 }
 
 // ----------------------------------------------------------------- top-k
@@ -941,14 +1098,16 @@ cudaError_t launch_idx_pipe(const IdxArgs& a, const CUtensorMap& map, unsigned i
   return cudaGetLastError();
 }
 
-template <int NT>
-cudaError_t launch_idx_tma(const IdxArgs& a, const CUtensorMap& map, unsigned int* fw, dim3 grid, size_t smem,
-                           cudaStream_t stream) {
+template <int H>
+cudaError_t launch_idx_tc(const IdxArgs& a, const CUtensorMap& map, unsigned int* fw, cudaStream_t stream) {
+  const size_t smem = sizeof(TcIdxSmem<H>) + 1024;
   static std::atomic<uint64_t> configured{0};
-  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(indexer_scores_tma_kernel<NT>),
+  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(indexer_scores_tc_kernel<H>),
                                       static_cast<int>(smem), &configured);
   if (e != cudaSuccess) return e;
-  indexer_scores_tma_kernel<NT><<<grid, kIdxWarps * 32, smem, stream>>>(a, map, fw);
+  const int64_t n_items = static_cast<int64_t>(a.batch) * ((a.max_ctx + kTcIdxChunk - 1) / kTcIdxChunk);
+  const int64_t grid = std::min<int64_t>(n_items, 2 * static_cast<int64_t>(device_sm_count()));
+  indexer_scores_tc_kernel<H><<<static_cast<unsigned>(grid), kTcIdxThreads, smem, stream>>>(a, map, fw);
   return cudaGetLastError();
 }
 
@@ -978,12 +1137,11 @@ cudaError_t launch_indexer_scores(const uint16_t* q_idx, const float* head_w, co
   if (fw != nullptr && num_blocks > 0 && block_stride % kIdxDim == 0 && rows <= 0x7FFFFFFF &&
       encode_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, key_pool, kIdxDim, rows, kIdxDim, kIdxDim, kBlock,
                            CU_TENSOR_MAP_SWIZZLE_128B)) {
-    const size_t smem = sizeof(IdxSmem) + 1024;
     switch (n_heads / 8) {
       case 1: return launch_idx_pipe<1>(a, map, fw, stream);
       case 2: return launch_idx_pipe<2>(a, map, fw, stream);
-      case 4: return launch_idx_pipe<4>(a, map, fw, stream);
-      case 8: return launch_idx_tma<8>(a, map, fw, grid, smem, stream);
+      case 4: return launch_idx_tc<32>(a, map, fw, stream);
+      case 8: return launch_idx_tc<64>(a, map, fw, stream);
       default: return cudaErrorInvalidValue;
     }
   }
