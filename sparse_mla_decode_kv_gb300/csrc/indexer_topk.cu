@@ -791,6 +791,11 @@ __device__ void select_and_compact(const Src& src, int count, int topk, int32_t*
   uint32_t prefix = 0, need = topk;
   const int shifts[3] = {21, 10, 0};
   const uint32_t widths[3] = {11, 11, 10};
+  // The passes resolve the k-th largest key 11, 11 and 10 bits at a time.
+  // Once the bin holding it contains exactly the `need` elements still to
+  // take, every element of the bin is taken and its lower bits do not
+  // matter: the selection stops there (prefix compared at `t_shift`).
+  int t_shift = 0;
   for (int pass = 0; pass < 3; ++pass) {
     for (int j = tid; j < kHistBins; j += kTopkThreads) sm.hist[j] = 0;
     __syncthreads();
@@ -817,7 +822,10 @@ __device__ void select_and_compact(const Src& src, int count, int topk, int32_t*
     const uint32_t bin = select_bin(sm.hist, need, sm.warp_sums, &sm.sel_bin, &sm.sel_need);
     need = sm.sel_need;
     prefix = (pass == 0) ? bin : ((prefix << widths[pass]) | bin);
+    const bool whole_bin = sm.hist[bin] == need;
+    t_shift = sh;
     __syncthreads();
+    if (whole_bin) break;
   }
   const uint32_t T = prefix;
   // element j goes to position G(j) + min(E(j), need), G / E counting keys > T / == T before j
@@ -830,7 +838,7 @@ __device__ void select_and_compact(const Src& src, int count, int topk, int32_t*
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
       const int j = base + tid * kPer + i;
-      keys[i] = j < count ? src.key(j) : 0u;
+      keys[i] = j < count ? (src.key(j) >> t_shift) : 0u;
       ngt += (j < count && keys[i] > T);
       neq += (j < count && keys[i] == T);
     }
@@ -880,6 +888,7 @@ constexpr int kPartThreads = 256;
 constexpr int kPartWarps = kPartThreads / 32;
 constexpr int kPartCap = kCandCap / kParts;          // 2,048 candidates per part
 constexpr int kPartWarpCap = kPartCap / kPartWarps;  // 256 per warp
+constexpr int kCollectSample = 2048;  // strided sample of the row that sets the threshold
 
 struct CollectSmem {
   uint32_t hist[kHistBins];
@@ -927,6 +936,9 @@ __global__ void __launch_bounds__(kPartThreads)
                         int topk, int max_ctx, uint32_t* __restrict__ cand_key, int32_t* __restrict__ cand_idx,
                         int32_t* __restrict__ cand_cnt) {
   __shared__ CollectSmem sm;
+  // The selection kernel is launched as a programmatic dependent of this
+  // one: it may become resident now and waits for this grid to complete.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int part = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n = max(0, min(__ldg(ctx_lens + b), max_ctx));
@@ -934,13 +946,13 @@ __global__ void __launch_bounds__(kPartThreads)
   const float* row = scores + static_cast<int64_t>(b) * row_stride;
 
   // 1. Threshold from the strided sample of the whole row.
-  uint32_t key[kSample / kPartThreads];
+  uint32_t key[kCollectSample / kPartThreads];
 #pragma unroll
-  for (int u = 0; u < kSample / kPartThreads; ++u) {
+  for (int u = 0; u < kCollectSample / kPartThreads; ++u) {
     const int i = tid + u * kPartThreads;
-    key[u] = order_key(__ldg(row + static_cast<int>((static_cast<int64_t>(i) * n) / kSample)));
+    key[u] = order_key(__ldg(row + static_cast<int>((static_cast<int64_t>(i) * n) / kCollectSample)));
   }
-  const int r0 = min(kSample - 1, static_cast<int>((2.5 * topk * kSample) / n) + 8);
+  const int r0 = min(kCollectSample - 1, static_cast<int>((2.5 * topk * kCollectSample) / n) + 8);
   uint32_t need = r0 + 1, prefix = 0;
 #pragma unroll 1
   for (int pass = 0; pass < 2; ++pass) {
@@ -948,7 +960,7 @@ __global__ void __launch_bounds__(kPartThreads)
     if (tid == 0) sm.sel_bin = sm.sel_need = 0;
     __syncthreads();
 #pragma unroll
-    for (int u = 0; u < kSample / kPartThreads; ++u) {
+    for (int u = 0; u < kCollectSample / kPartThreads; ++u) {
       if (pass == 0) hist_add(sm.hist, key[u] >> 21, true);
       else hist_add(sm.hist, (key[u] >> 10) & 0x7FFu, (key[u] >> 21) == prefix);
     }
@@ -1014,6 +1026,9 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
                                                             const int32_t* __restrict__ cand_idx,
                                                             const int32_t* __restrict__ cand_cnt,
                                                             int32_t* __restrict__ out) {
+  // A programmatic dependent of the collection kernel: nothing is read
+  // before that grid has completed and its candidate lists are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   extern __shared__ __align__(16) uint8_t topk_smem_raw[];
   TopkSmem& sm = *reinterpret_cast<TopkSmem*>(topk_smem_raw);
   const int b = blockIdx.x;
@@ -1043,14 +1058,35 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
     select_and_compact(RowSrc{row}, n, topk, orow, sm);
     return;
   }
-  int off = 0;
+  // Candidate j of the concatenation lies in the last part whose start is
+  // <= j; each thread issues all its loads before storing any (one L2 round
+  // trip for the whole list instead of one per part).
+  int start[kParts];
+  start[0] = 0;
 #pragma unroll
-  for (int p = 0; p < kParts; ++p) {
-    for (int e = tid; e < cnt[p]; e += kTopkThreads) {
-      sm.cand_key[off + e] = __ldg(cand_key + (slot0 + p) * kPartCap + e);
-      sm.cand_idx[off + e] = __ldg(cand_idx + (slot0 + p) * kPartCap + e);
+  for (int p = 1; p < kParts; ++p) start[p] = start[p - 1] + cnt[p - 1];
+  constexpr int kLoadsPerThread = 4;
+  for (int base = 0; base < total; base += kLoadsPerThread * kTopkThreads) {
+    uint32_t kv[kLoadsPerThread];
+    int32_t iv[kLoadsPerThread];
+#pragma unroll
+    for (int u = 0; u < kLoadsPerThread; ++u) {
+      const int j = base + u * kTopkThreads + tid;
+      int p = 0;
+#pragma unroll
+      for (int q = 1; q < kParts; ++q) p += j >= start[q];
+      const int64_t src = (slot0 + p) * kPartCap + (j - start[p]);
+      kv[u] = j < total ? __ldg(cand_key + src) : 0u;
+      iv[u] = j < total ? __ldg(cand_idx + src) : 0;
     }
-    off += cnt[p];
+#pragma unroll
+    for (int u = 0; u < kLoadsPerThread; ++u) {
+      const int j = base + u * kTopkThreads + tid;
+      if (j < total) {
+        sm.cand_key[j] = kv[u];
+        sm.cand_idx[j] = iv[u];
+      }
+    }
   }
   __syncthreads();
   select_and_compact(CandSrc{&sm}, total, topk, orow, sm);
@@ -1080,9 +1116,22 @@ cudaError_t launch_topk(const float* scores, int64_t row_stride, const int32_t* 
                                                                        max_context_len, cand_key, cand_idx, cand_cnt);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  topk_kernel<<<batch, kTopkThreads, sizeof(TopkSmem), stream>>>(scores, row_stride, context_lens, topk,
-                                                                  max_context_len, cand_key, cand_idx, cand_cnt, out);
-  return cudaGetLastError();
+  // the selection as a programmatic dependent: its launch overlaps the tail
+  // of the collection (it waits for the whole grid before reading)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(batch);
+  cfg.blockDim = dim3(kTopkThreads);
+  cfg.dynamicSmemBytes = sizeof(TopkSmem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, topk_kernel, scores, row_stride, context_lens, topk, max_context_len,
+                         static_cast<const uint32_t*>(cand_key), static_cast<const int32_t*>(cand_idx),
+                         static_cast<const int32_t*>(cand_cnt), out);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int NT>
