@@ -418,7 +418,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
 // x heads, so one MMA chain gives both partial dot products of every head:
 // D[t, h] + D[t, H + h] = 2^k_h (q_h . k_t) for the 128 tokens t of a chunk
 // (M = 128, four K = 32 steps over the 128 dims).  Roles: warp 4 loads key
-// tiles and scales into a four-slot ring (as the pipelined kernel); warp 5
+// tiles and scales into a three-slot ring (as the pipelined kernel); warp 5
 // owns the tensor memory (two accumulators of N columns) and one of its
 // lanes issues the MMAs; warps 0-3 -- tensor-memory lanes 0-127, one token
 // each -- read the accumulator, apply relu, the token scale and the head
@@ -426,7 +426,11 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
 // the request changes.
 constexpr int kTcIdxChunk = 128;                    // tokens per chunk = MMA M
 constexpr int kTcIdxBlocks = kTcIdxChunk / kBlock;  // 2 key blocks
-constexpr int kTcIdxSlots = 4;
+constexpr int kTcIdxSlots = 3;
+// CTAs per SM: three for 32 heads (60 KB of shared memory and 128
+// tensor-memory columns each); two for 64 heads, whose 256 columns per CTA
+// would not fit three times in an SM's 512.
+__host__ __device__ constexpr int tc_idx_ctas_per_sm(int heads) { return heads <= 32 ? 3 : 2; }
 constexpr int kTcIdxEpiWarps = 4;
 constexpr int kTcIdxThreads = (kTcIdxEpiWarps + 2) * 32;
 constexpr int kTcIdxItemsPerLookup = 32 / kTcIdxBlocks;
@@ -444,7 +448,7 @@ struct alignas(1024) TcIdxSmem {
 };
 
 template <int H>
-__global__ void __launch_bounds__(kTcIdxThreads, 2)
+__global__ void __launch_bounds__(kTcIdxThreads, tc_idx_ctas_per_sm(H))
     indexer_scores_tc_kernel(const IdxArgs a, const __grid_constant__ CUtensorMap tmap, unsigned int* fault_word) {
   constexpr int N = 2 * H;                                  // accumulator columns per chunk
   constexpr uint32_t kCols = 2 * N;                         // two accumulators
@@ -1155,7 +1159,8 @@ cudaError_t launch_idx_tc(const IdxArgs& a, const CUtensorMap& map, unsigned int
                                       static_cast<int>(smem), &configured);
   if (e != cudaSuccess) return e;
   const int64_t n_items = static_cast<int64_t>(a.batch) * ((a.max_ctx + kTcIdxChunk - 1) / kTcIdxChunk);
-  const int64_t grid = std::min<int64_t>(n_items, 2 * static_cast<int64_t>(device_sm_count()));
+  const int64_t grid =
+      std::min<int64_t>(n_items, tc_idx_ctas_per_sm(H) * static_cast<int64_t>(device_sm_count()));
   indexer_scores_tc_kernel<H><<<static_cast<unsigned>(grid), kTcIdxThreads, smem, stream>>>(a, map, fw);
   return cudaGetLastError();
 }
