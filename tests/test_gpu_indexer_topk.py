@@ -182,3 +182,40 @@ def test_indexer_key_stride_not_a_multiple_of_128():
     idx, sc = run_indexer(m, wl, 4000)
     for b in range(3):
         check_request(idx[b], sc[b], ref[b], wl.topk)
+
+
+@pytest.mark.parametrize("nh", [32, 64])
+def test_indexer_query_far_below_its_maximum(nh):
+    """The tensor-core indexer represents each head's query as two e4m3 parts
+    after scaling its largest magnitude into [128, 256): every element is
+    exact to within 2^-10 of the scaled unit, i.e. max|q_h| / 128 * 2^-10
+    before scaling.  A query with one large element per head and every other
+    element 10^-6 .. 10^-2 of it puts most elements in that subnormal range;
+    relu is 1-Lipschitz, so every score is within
+    sum_h w_h * s_t * sum_d |k_t,d| * max|q_h| / 128 * 2^-10 of the float64
+    score, plus the float32 tolerance.  The top-k is exact on the GPU's own
+    scores."""
+    m = lib()
+    lens = [3000, 1000]
+    wl = W.indexer_keys(DEV, seed=11 + nh, batch=2, n_heads=nh, topk=256, ctx_lens=lens)
+    rng = np.random.default_rng(nh)
+    q = rng.standard_normal((2, nh, 128)) * 10.0 ** rng.uniform(-6, -2, (2, nh, 128))
+    q[:, :, 0] = rng.choice([-1.0, 1.0], (2, nh)) * 10.0 ** rng.uniform(0, 2, (2, nh))
+    wl.q_idx = torch.from_numpy(q.astype(np.float32)).to(torch.bfloat16).to(DEV).contiguous()
+    idx, sc = run_indexer(m, wl, max(lens))
+    ref = oracle_scores(wl, None, 1)
+    qb = wl.q_idx.float().cpu().numpy().astype(np.float64)
+    w = wl.head_w.cpu().numpy().astype(np.float64)
+    err_q = np.abs(qb).max(axis=2) / 128.0 * 2.0 ** -10  # [B, H]: largest representation error
+    pool = wl.key_pool.view(-1, wl.key_stride)
+    bt = wl.block_table.cpu().numpy()
+    for b, c in enumerate(lens):
+        nblk = (c + 63) // 64
+        blocks = pool[torch.from_numpy(bt[b, :nblk].astype(np.int64)).to(DEV)]
+        codes = blocks[:, :64 * 128].contiguous().view(torch.float8_e4m3fn).float().view(nblk * 64, 128)
+        scale = blocks[:, 64 * 128:64 * 132].contiguous().view(torch.float32).reshape(nblk * 64)
+        kabs = (codes.abs().sum(dim=1) * scale).cpu().numpy().astype(np.float64)[:c]  # sum_d |k_t,d| s_t
+        bound = kabs * float(np.dot(w[b], err_q[b])) + 1e-5 * (1 + np.abs(ref[b][:c]))
+        diff = np.abs(sc[b, :c].astype(np.float64) - ref[b][:c])
+        assert np.all(diff <= bound), f"request {b}: worst excess {np.max(diff - bound):.3e}"
+        assert np.array_equal(idx[b], lexsort_topk(sc[b, :c], wl.topk)), "top-k of the GPU's scores"
