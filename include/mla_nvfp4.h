@@ -145,8 +145,10 @@ mla_status_t mla_index_key_quantize_append(const uint16_t* keys, const int64_t* 
  *   lse[b,h] = log sum_t exp(z[h,t])                   (natural log, float)
  *
  * An empty V_b gives out = 0 and lse = -inf.  Arithmetic: FP16 tensor-core
- * operands (the dequantized values are exact in FP16; q is converted from
- * bf16 with saturation at +-65504) and FP32 accumulation and softmax; when
+ * operands (the dequantized values are exact in FP16; each head's q is
+ * scaled by a power of two into [2^14, 2^15) before its bf16 -> FP16
+ * conversion, the inverse folded into that head's softmax scale, so any
+ * finite bf16 query is accepted) and FP32 accumulation and softmax; when
  * the list is split over several CTAs (mla_sparse_decode_plan), each split's
  * normalised partial output is rounded to FP16 in the workspace before the
  * FP32 LSE-weighted merge.
@@ -353,9 +355,16 @@ mla_status_t mla_topk(const float* scores, int64_t score_row_stride, const int32
  *
  * where k_t is the token's 128 e4m3 key values and s_t its float scale
  * ("GLM-5.3 PCP/DCP long-context on H200", section 3: a key is 128 e4m3
- * bytes and a float scale); then topk_out = mla_topk(score).  Tensor-core
- * products use FP16 operands (keys exact; q converted from bf16 with
- * saturation) with FP32 accumulation.
+ * bytes and a float scale); then topk_out = mla_topk(score).  The products
+ * run on the tensor cores with FP32 accumulation.  Each head's query is
+ * first scaled by a power of two 2^k_h and its weight by 2^-k_h (exact:
+ * relu is positively homogeneous), so any finite bf16 query is accepted.
+ * With 32 or 64 index heads and a block stride that is a multiple of 128
+ * bytes the operands are e4m3: the keys as stored, the query scaled into
+ * [128, 256) and split into two e4m3 parts (an element is represented to
+ * within max|q_h| 2^-17).  Otherwise they are FP16: the keys exact, the
+ * query scaled into [2^14, 2^15) (exact for elements above 2^-10 of the
+ * head's largest, FP16 subnormals below that).
  *
  *   q_idx         device bf16 [batch, n_idx_heads, 128]
  *   head_w        device float [batch, n_idx_heads]

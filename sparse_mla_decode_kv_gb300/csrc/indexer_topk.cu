@@ -45,9 +45,10 @@ constexpr int kIdxWarps = 4;
 constexpr int kIdxTokensPerCta = 512;
 constexpr int kIdxBlockBytesKeys = kBlock * kIdxDim;  // 8,192 key bytes, then 64 float scales
 
-__device__ __forceinline__ uint32_t bf16pair_to_f16x2(uint32_t two) {
-  return f32x2_to_f16x2_sat(bf16_bits_to_f32(two & 0xFFFFu), bf16_bits_to_f32(two >> 16));
+__device__ __forceinline__ uint32_t bf16pair_to_f16x2(uint32_t two, float mul) {
+  return f32x2_to_f16x2_sat(bf16_bits_to_f32(two & 0xFFFFu) * mul, bf16_bits_to_f32(two >> 16) * mul);
 }
+
 
 struct IdxArgs {
   const uint16_t* q;
@@ -65,6 +66,44 @@ struct IdxArgs {
   int batch;
 };
 
+// The query of request b as mma.sync B fragments (K = 128 dims permuted like
+// the keys, N = 8 NT heads) in FP16, and the head weights of this lane's
+// epilogue heads (8n + 2c, 8n + 2c + 1).  The bf16 query does not fit FP16's
+// exponent range in general, so each head is scaled by a power of two 2^k
+// that brings its largest magnitude into [2^14, 2^15) and its weight by 2^-k:
+// w relu(s 2^k dot) 2^-k = w relu(s dot), exactly.  Lane (g, c) holds dims
+// 32q + 8c .. + 8 of head 8n + g; the four lanes of a head reduce its maximum.
+template <int NT>
+__device__ __forceinline__ void load_query_fragments(const IdxArgs& a, int b, int g, int c,
+                                                     uint32_t (&bq)[8][NT][2], float (&wh)[NT][2]) {
+  const float* wb = a.w + static_cast<int64_t>(b) * a.n_heads;
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+    const uint16_t* qh = a.q + (static_cast<int64_t>(b) * a.n_heads + 8 * n + g) * kIdxDim;
+    uint4 v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[q] = __ldg(reinterpret_cast<const uint4*>(qh + 32 * q + 8 * c));
+    uint32_t m = max(max(bf16x8_absmax_bits(v[0]), bf16x8_absmax_bits(v[1])),
+                     max(bf16x8_absmax_bits(v[2]), bf16x8_absmax_bits(v[3])));
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+    const int k = query_shift(m);
+    const float mul = pow2f(k);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      bq[2 * q][n][0] = bf16pair_to_f16x2(v[q].x, mul);
+      bq[2 * q][n][1] = bf16pair_to_f16x2(v[q].y, mul);
+      bq[2 * q + 1][n][0] = bf16pair_to_f16x2(v[q].z, mul);
+      bq[2 * q + 1][n][1] = bf16pair_to_f16x2(v[q].w, mul);
+    }
+    // the shifts of heads 8n + 2c and 8n + 2c + 1 (held by lanes 4 (2c) and 4 (2c + 1))
+    const int k0 = __shfl_sync(0xFFFFFFFFu, k, 8 * c);
+    const int k1 = __shfl_sync(0xFFFFFFFFu, k, 8 * c + 4);
+    wh[n][0] = __ldg(wb + 8 * n + 2 * c) * pow2f(-k0);
+    wh[n][1] = __ldg(wb + 8 * n + 2 * c + 1) * pow2f(-k1);
+  }
+}
+
 // Row address of token t's key (nullptr when masked) and its scale.
 __device__ __forceinline__ const uint8_t* key_row(const IdxArgs& a, const int32_t* bt_row, int t, int ctx,
                                                   float* scale) {
@@ -78,8 +117,8 @@ __device__ __forceinline__ const uint8_t* key_row(const IdxArgs& a, const int32_
   return blk + (t % kBlock) * kIdxDim;
 }
 
-template <int NT>  // n-tiles of 8 heads
-__global__ void __launch_bounds__(kIdxWarps * 32, 3) indexer_scores_kernel(const IdxArgs a) {
+template <int NT>  // n-tiles of 8 heads (64 heads: two CTAs per SM, their query fragments take 128 registers)
+__global__ void __launch_bounds__(kIdxWarps * 32, NT == 8 ? 2 : 3) indexer_scores_kernel(const IdxArgs a) {
   const int b = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
@@ -91,22 +130,7 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 3) indexer_scores_kernel(const
   // Query B fragments (K = 128 dims permuted like the keys, N = 8*NT heads) and head weights.
   uint32_t bq[8][NT][2];
   float wh[NT][2];
-#pragma unroll
-  for (int n = 0; n < NT; ++n) {
-    const int h = 8 * n + g;
-    const uint16_t* qh = a.q + (static_cast<int64_t>(b) * a.n_heads + h) * kIdxDim;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(qh + 32 * q + 8 * c));
-      bq[2 * q][n][0] = bf16pair_to_f16x2(v.x);
-      bq[2 * q][n][1] = bf16pair_to_f16x2(v.y);
-      bq[2 * q + 1][n][0] = bf16pair_to_f16x2(v.z);
-      bq[2 * q + 1][n][1] = bf16pair_to_f16x2(v.w);
-    }
-    const float* wb = a.w + static_cast<int64_t>(b) * a.n_heads;
-    wh[n][0] = __ldg(wb + 8 * n + 2 * c);
-    wh[n][1] = __ldg(wb + 8 * n + 2 * c + 1);
-  }
+  load_query_fragments<NT>(a, b, g, c, bq, wh);
 
   float* out_row = a.scores + static_cast<int64_t>(b) * a.scores_stride;
   const int n_mt = kIdxTokensPerCta / 16;
@@ -304,21 +328,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
       // the request's query (B fragments, K permuted like the keys) and head weights
       cur_b = b;
       ctx = min(__ldg(a.ctx_lens + b), a.max_ctx);
-#pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        const uint16_t* qh = a.q + (static_cast<int64_t>(b) * a.n_heads + 8 * n + g) * kIdxDim;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(qh + 32 * q + 8 * c));
-          bq[2 * q][n][0] = bf16pair_to_f16x2(v.x);
-          bq[2 * q][n][1] = bf16pair_to_f16x2(v.y);
-          bq[2 * q + 1][n][0] = bf16pair_to_f16x2(v.z);
-          bq[2 * q + 1][n][1] = bf16pair_to_f16x2(v.w);
-        }
-        const float* wb = a.w + static_cast<int64_t>(b) * a.n_heads;
-        wh[n][0] = __ldg(wb + 8 * n + 2 * c);
-        wh[n][1] = __ldg(wb + 8 * n + 2 * c + 1);
-      }
+      load_query_fragments<NT>(a, b, g, c, bq, wh);
     }
     if (chunk * kPipeChunk >= ctx) continue;
     const int slot = s % kPipeSlots;

@@ -219,3 +219,33 @@ def test_indexer_query_far_below_its_maximum(nh):
         diff = np.abs(sc[b, :c].astype(np.float64) - ref[b][:c])
         assert np.all(diff <= bound), f"request {b}: worst excess {np.max(diff - bound):.3e}"
         assert np.array_equal(idx[b], lexsort_topk(sc[b, :c], wl.topk)), "top-k of the GPU's scores"
+
+
+@pytest.mark.parametrize("padded", [False, True], ids=["tma", "padded"])
+@pytest.mark.parametrize("nh", [8, 16, 32, 64])
+@pytest.mark.parametrize("factor", [2.0 ** 20, 2.0 ** -24], ids=["2^20", "2^-24"])
+def test_indexer_query_outside_fp16_range(nh, factor, padded):
+    """q times f with the head weights divided by f gives the same scores
+    (relu is positively homogeneous), but puts the query beyond FP16's
+    largest value (2^20) or below its normal range (2^-24).  Every score
+    kernel -- tensor-memory (32, 64 heads), pipelined (8, 16) and the one for
+    key strides TMA cannot tile (padded) -- scales each head by a power of two
+    and must still match the float64 oracle within the score tolerance."""
+    m = lib()
+    lens = [2500, 700]
+    wl = W.indexer_keys(DEV, seed=23 + nh, batch=2, n_heads=nh, topk=256, ctx_lens=lens)
+    wl.q_idx = (wl.q_idx.double() * factor).to(torch.bfloat16).contiguous()
+    wl.head_w = (wl.head_w.double() / factor).float().contiguous()
+    if padded:
+        pad = wl.key_stride + 16
+        pool = torch.zeros(wl.num_blocks * pad, dtype=torch.uint8, device=DEV)
+        pool.view(wl.num_blocks, pad)[:, :wl.key_stride] = wl.key_pool.view(wl.num_blocks, wl.key_stride)
+        ref = oracle_scores(wl, None, 1)
+        wl.key_pool, wl.key_stride = pool, pad
+    else:
+        ref = oracle_scores(wl, None, 1)
+    idx, sc = run_indexer(m, wl, max(lens))
+    for b, c in enumerate(lens):
+        diff = np.abs(sc[b, :c].astype(np.float64) - ref[b][:c])
+        assert np.all(diff <= SCORE_TOL * (1 + np.abs(ref[b][:c]))), f"request {b}: max diff {diff.max():.3e}"
+        assert np.array_equal(idx[b], lexsort_topk(sc[b, :c], wl.topk)), "top-k of the GPU's scores"
