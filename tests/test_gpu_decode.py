@@ -93,12 +93,14 @@ def test_small_shapes(fmt, batch, heads, topk, ctx_lens):
 
 
 @pytest.mark.parametrize("fmt", FMTS)
-def test_masked_duplicates_and_bad_blocks(fmt):
+@pytest.mark.parametrize("heads", [16, 64])
+def test_masked_duplicates_and_bad_blocks(fmt, heads):
     """-1 entries, positions past the context, duplicates, unsorted lists, a
     block id outside the pool and a logical block past the table are all
-    handled on the device without faults."""
+    handled on the device without faults (64 heads on NVFP4: the
+    tensor-memory kernel)."""
     m = lib()
-    wl = small_workload(3, 16, 512, [3000, 3000, 700], seed=77)
+    wl = small_workload(3, heads, 512, [3000, 3000, 700], seed=77)
     W.fill_pool(wl, fmt, quantize_fn(m))
     rng = np.random.default_rng(5)
     idx = wl.topk_idx.cpu().numpy().copy()
