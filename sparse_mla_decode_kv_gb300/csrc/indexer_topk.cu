@@ -21,7 +21,7 @@
 //
 // Top-k in two kernels.  Scores map to order-preserving 32-bit keys (with
 // -0.0 folded into +0.0).  topk_collect_kernel: 8 CTAs per request each draw
-// the same strided sample of 2,048 keys of the whole row, take from it a
+// the same sample of 2,048 keys of the whole row (256 runs of 8), take from it a
 // threshold expected to keep ~2.5 k elements (two radix passes over the
 // sample), and collect the elements of their eighth of the row at or above
 // it into global lists in index order.  topk_kernel: one 1,024-thread CTA
@@ -772,14 +772,10 @@ __device__ __forceinline__ uint32_t select_bin(const uint32_t* hist, uint32_t ne
   return *sel_bin;
 }
 
-// Sample-select parameters: a strided sample of kSample keys fixes a
-// threshold T0 expected to keep ~2.5 k elements; one order-preserving pass
-// collects every element >= T0 into per-warp lists (warp w scans a contiguous
-// chunk, so concatenating the lists keeps index order); the exact selection
-// then runs on the candidates in shared memory.  If a list overflows or fewer
-// than k elements reach T0, the kernel falls back to radix passes over the
-// whole row.
-constexpr int kSample = 2048;
+// Selection kernel: the candidates every collection CTA kept (keys >= the
+// sample threshold T0, in index order) are concatenated in shared memory and
+// the exact selection runs on them.  If a list overflowed or fewer than k
+// elements reached T0, it falls back to radix passes over the whole row.
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kWarpCap = 512;
 constexpr int kCandCap = kWarpCap * kTopkWarps;  // 16,384 candidates
@@ -787,7 +783,6 @@ constexpr int kCandCap = kWarpCap * kTopkWarps;  // 16,384 candidates
 struct TopkSmem {
   uint32_t cand_key[kCandCap];
   int32_t cand_idx[kCandCap];
-  uint32_t sample[kSample];
   uint32_t hist[kHistBins];
   uint32_t warp_sums[32];
   uint32_t warp_cnt[32];
@@ -892,7 +887,7 @@ struct CandSrc {
 };
 
 // ---- parallel candidate collection: kParts CTAs per request ---------------
-// Every part CTA draws the same strided sample of the whole row and takes
+// Every part CTA draws the same sample of the whole row and takes
 // the same threshold T0 from it (two radix passes over the sample give the
 // lower bound of the 22-bit key bin holding the sample's r0-th largest key);
 // it then collects its part's elements with key >= T0, in index order, into
@@ -902,7 +897,7 @@ constexpr int kPartThreads = 256;
 constexpr int kPartWarps = kPartThreads / 32;
 constexpr int kPartCap = kCandCap / kParts;          // 2,048 candidates per part
 constexpr int kPartWarpCap = kPartCap / kPartWarps;  // 256 per warp
-constexpr int kCollectSample = 2048;  // strided sample of the row that sets the threshold
+constexpr int kCollectSample = 2048;  // sample of the row that sets the threshold (256 runs of 8)
 
 struct CollectSmem {
   uint32_t hist[kHistBins];
@@ -959,12 +954,19 @@ __global__ void __launch_bounds__(kPartThreads)
   if (n <= topk) return;  // the selection kernel takes everything
   const float* row = scores + static_cast<int64_t>(b) * row_stride;
 
-  // 1. Threshold from the strided sample of the whole row.
+  // 1. Threshold from a sample of the whole row: 256 runs of 8 consecutive
+  // scores spread evenly over it.  Eight lanes read one run (one 32-byte
+  // sector), so the sample costs 256 sector requests per CTA rather than
+  // 2,048 scattered ones (all parts of a request draw the same sample).
   uint32_t key[kCollectSample / kPartThreads];
+  {
+    constexpr int kRuns = kCollectSample / 8;
 #pragma unroll
-  for (int u = 0; u < kCollectSample / kPartThreads; ++u) {
-    const int i = tid + u * kPartThreads;
-    key[u] = order_key(__ldg(row + static_cast<int>((static_cast<int64_t>(i) * n) / kCollectSample)));
+    for (int u = 0; u < kCollectSample / kPartThreads; ++u) {
+      const int r = (tid >> 3) + (kPartThreads / 8) * u;
+      const int pos = static_cast<int>((static_cast<int64_t>(r) * n) / kRuns) & ~7;
+      key[u] = order_key(__ldg(row + min(pos + (tid & 7), n - 1)));
+    }
   }
   const int r0 = min(kCollectSample - 1, static_cast<int>((2.5 * topk * kCollectSample) / n) + 8);
   uint32_t need = r0 + 1, prefix = 0;
