@@ -82,7 +82,7 @@ def peaks():
 # of the kernel source it was taken on: once the source differs, the figure
 # no longer describes the kernel and is reported as null.
 E2E_CHUNKS = 4  # copy chunks per step of the end-to-end pass
-DECODE_NVFP4_TRAFFIC = {"bytes": 29_498_112 + 512, "source_digest": "cbbf79e10b0d197c"}
+DECODE_NVFP4_TRAFFIC = {"bytes": 29_498_112 + 2_304, "source_digest": "0fad475c4951d847"}
 KERNEL_SOURCES = ("sparse_mla_decode_kv_gb300/csrc/sparse_decode.cu", "sparse_mla_decode_kv_gb300/csrc/mla_device.cuh")
 
 

@@ -27,9 +27,12 @@ constexpr int kIdxDim = 128;               // indexer key width (e4m3)
 // mla_api.cu whose address kernels receive as an argument).
 constexpr unsigned int kFaultDecodeWait = 1u;
 constexpr unsigned int kFaultIndexerWait = 2u;
-// Poll budget of the back-off phase of a bounded wait (each poll sleeps up to
-// ~1 us): seconds in total, far beyond any legitimate wait in these kernels.
-constexpr uint32_t kWaitPolls = 1u << 22;
+// Poll budget of the back-off phase of a bounded wait (each poll sleeps a
+// few microseconds): about a second in total, with the hinted phase before
+// it, far beyond any legitimate wait in these kernels (microseconds).  Polls
+// do not advance while the context is switched out, so time-slicing with
+// other work does not make a wait give up early.
+constexpr uint32_t kWaitPolls = 1u << 18;
 
 // ---- conversions -----------------------------------------------------------
 // Two e2m1 codes (low nibble -> low half) to two exact f16 values.
