@@ -81,7 +81,25 @@ def peaks():
 # -s 1 -c 1` on `bench.py --ctx 16384 --layers 2 --no-extras`), and a digest
 # of the kernel source it was taken on: once the source differs, the figure
 # no longer describes the kernel and is reported as null.
-E2E_CHUNKS = 4  # copy chunks per step of the end-to-end pass
+
+
+def e2e_chunks(n_layers):
+    """Layers per copy chunk of the end-to-end pass: small chunks at both ends
+    (the first chunk's inputs and the last chunk's outputs are the copies no
+    decode hides), chunks of at most six layers in between; 1, 2, 4, 6, 6, 3, 1
+    for 23 layers."""
+    head, tail, rest = [], [], n_layers
+    for s in (1, 2, 4):
+        if rest > s + 4:
+            head.append(s)
+            rest -= s
+    for s in (1, 3):
+        if rest > s + 4:
+            tail.insert(0, s)
+            rest -= s
+    n_mid = max(1, -(-rest // 6)) if rest > 0 else 0
+    mid = [rest // n_mid + (1 if i < rest % n_mid else 0) for i in range(n_mid)]
+    return head + mid + tail
 DECODE_NVFP4_TRAFFIC = {"bytes": 29_498_112 + 2_304, "source_digest": "0fad475c4951d847"}
 KERNEL_SOURCES = ("sparse_mla_decode_kv_gb300/csrc/sparse_decode.cu", "sparse_mla_decode_kv_gb300/csrc/mla_device.cuh")
 
@@ -513,10 +531,13 @@ def main():
     h2d = in_bytes * L
     d2h = out_bytes * L
 
-    # The step's layers in E2E_CHUNKS chunks: a second stream copies chunk
-    # c + 1's inputs and chunk c - 1's outputs while chunk c decodes.
-    n_chunks = min(E2E_CHUNKS, L)
-    bounds = [(L * c // n_chunks, L * (c + 1) // n_chunks) for c in range(n_chunks)]
+    # The step's layers in chunks (e2e_chunks): a second stream copies the
+    # inputs of the chunks ahead and the outputs of the chunks done while a
+    # chunk decodes.
+    bounds, lo = [], 0
+    for n in e2e_chunks(L):
+        bounds.append((lo, lo + n))
+        lo += n
     copy_stream = torch.cuda.Stream(device=dev)
 
     def e2e_step():
