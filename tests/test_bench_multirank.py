@@ -71,3 +71,16 @@ def test_reference_arm_other_ranks_do_no_work(capsys):
 
     assert bench.run_reference(Args, 1, 2) is None
     assert capsys.readouterr().out == ""
+
+
+@pytest.mark.parametrize("n_layers", [1, 2, 5, 8, 9, 12, 23, 40, 78])
+def test_e2e_copy_chunks_cover_every_layer_once(n_layers):
+    """The end-to-end pass copies every layer's inputs and outputs exactly
+    once per step, in chunks of at most six layers, and for the default 23
+    layers starts and ends with one-layer chunks (the copies no decode hides)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    chunks = bench.e2e_chunks(n_layers)
+    assert sum(chunks) == n_layers and min(chunks) >= 1 and max(chunks) <= 6 or n_layers <= 6
+    if n_layers == 23:
+        assert chunks[0] == 1 and chunks[-1] == 1
