@@ -81,6 +81,7 @@ def test_e2e_copy_chunks_cover_every_layer_once(n_layers):
     sys.path.insert(0, ROOT)
     import bench
     chunks = bench.e2e_chunks(n_layers)
-    assert sum(chunks) == n_layers and min(chunks) >= 1 and max(chunks) <= 6 or n_layers <= 6
+    assert sum(chunks) == n_layers and min(chunks) >= 1
+    assert max(chunks) <= max(6, n_layers if n_layers <= 6 else 6)
     if n_layers == 23:
         assert chunks[0] == 1 and chunks[-1] == 1
