@@ -17,6 +17,10 @@
 //  * indexer_scores_kernel (other strides): one CTA = 4 warps over 512 tokens
 //    of one request, keys loaded straight from the paged pool one m-tile
 //    ahead, mma.sync.
+// The two mma.sync kernels take the query as FP16 after scaling each head by
+// a power of two 2^k (its largest magnitude into [2^14, 2^15)) and its weight
+// by 2^-k, which leaves every score unchanged (relu is positively
+// homogeneous) and keeps the whole bf16 range.
 // All are HBM-bound at 132 bytes per token.
 //
 // Top-k in two kernels.  Scores map to order-preserving 32-bit keys (with
